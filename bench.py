@@ -1,0 +1,485 @@
+"""Benchmark: packed-state AdamW on GB300 (one JSON line on rank 0).
+
+Workload (default): the full TinyLlama-1.1B shape in the 16 B/param mixed
+layout (bf16 G | fp32 master | fp32 m | fp32 v | bf16 W), 24 blocks
+(embedding, 22 decoder layers, final norm + head), 1,100,048,384 parameters,
+17.6 GB of state; AdamW lr 1e-4, betas 0.9/0.999, eps 1e-8, wd 0.01.
+Inputs: the seeded synthetic generator (synth), step t starting at 1 with
+zero moments.
+
+  value     params/s of the device-resident step (lst_adamw_step, one
+            multi-block launch per step) with all state resident in HBM;
+            17.6 GB per launch, larger than L2, so no flush is needed.
+  e2e       params/s of the streamed step (lst_stream_step) over pinned
+            host blocks: every step copies the fields the update reads host
+            -> device and the fields it writes device -> host.
+  roofline  the fused update kernel against the measured HBM copy bandwidth.
+  stream    pinned host-link bandwidth measured in the same run (H2D, D2H,
+            both at once) and the streamed step against it.
+  cpu_baseline  the oracle (plain C, all host cores) on a bounded sample.
+
+`--impl reference` times the oracle alone on the host, on the same workload.
+Under torchrun (N > 1) every rank runs its own replica of the workload on its
+own GPU (weak scaling, no collective on the data path); value is the sum over
+ranks of parameters updated divided by the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "AdamW params/s/GPU; HBM GB/s % of peak; streamed host-link GB/s % of measured"
+WORKLOADS = {
+    # name: (shape function name, format, description)
+    "tinyllama_full_l16m": ("tinyllama_full", "L16M",
+                            "TinyLlama-1.1B full shape, 16 B/param mixed (fp32 master), 24 blocks"),
+    "tinyllama_layer_l12": ("tinyllama_layer", "L12", "one TinyLlama-1.1B decoder layer, 12 B/param"),
+    "tinyllama_lora_l16f": ("tinyllama_lora", "L16F", "TinyLlama-1.1B LoRA r=8 adapters, fp32, 22 blocks"),
+    "llama7b_l12": ("llama7b", "L12", "LLaMA-7B shape, 12 B/param, 34 blocks"),
+}
+# Algorithmic bytes per parameter of one device-resident step (reads + writes).
+ALG_BYTES = {"L12": 22, "L16M": 28, "L16F": 28}
+HP = dict(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+HP_LORA = dict(lr=2e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (host logic; covered by the gloo tests)
+# ---------------------------------------------------------------------------
+def dist_env():
+    """(rank, local_rank, world) from torchrun's environment, (0, 0, 1) otherwise."""
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, _, world = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(seed: int, rank: int) -> int:
+    """Each rank's replica draws its own state (weak scaling: a disjoint shard
+    of an N-times larger job)."""
+    return seed + 1_000_003 * rank
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_traffic(params: int):
+    """DRAM bytes per launch of the update kernel from the committed ncu
+    summary, scaled to `params`; None if the kernel source changed since."""
+    src = os.path.join(ROOT, "optimizer_update_gb300", "csrc", "lst_kernels.cu")
+    summ = os.path.join(ROOT, "profiles", "lst_update_kernel_traffic.txt")
+    if not os.path.exists(summ):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(summ):
+        p = line.split()
+        if len(p) >= 2 and not line.startswith("#"):
+            vals[p[0]] = p[1]
+    if vals.get("kernel_source_sha256_16") != sha:
+        return None
+    per_param = float(vals["dram_bytes_per_param"])
+    return per_param * params
+
+
+def build_layout(workload: str, max_blocks: int = 0):
+    """The workload's layout; max_blocks > 0 keeps only its first blocks (a
+    smaller case of the same kernel, e.g. for profiling)."""
+    from synth import shapes
+    from optimizer_update_gb300 import Layout
+    fn, fmt, _ = WORKLOADS[workload]
+    specs = getattr(shapes, fn)()
+    if max_blocks > 0:
+        specs = [s for s in specs if s[2] < max_blocks]
+    return Layout(specs, fmt)
+
+
+def alloc_pinned_state(L, workload: str, seed: int):
+    import ctypes
+    import numpy as np
+    import synth
+    from optimizer_update_gb300 import lst
+    ptrs, arrs = [], []
+    for i in range(L.n_layers):
+        n = L.block_bytes(i)
+        p = lst.lst_host_alloc(n)
+        a = np.ctypeslib.as_array((ctypes.c_uint8 * n).from_address(p))
+        synth.fill_block(L.numpy_views(i, a), L.spans(i), i, workload, L.fmt, t=1, seed=seed)
+        ptrs.append(p)
+        arrs.append(a)
+    return ptrs, arrs
+
+
+def cpu_oracle_rate(L, arrs, hp_kw, budget_s: float, threads: int):
+    """Oracle throughput (params/s) over the state, whole passes until the time
+    budget is used (at least one block)."""
+    import oracle
+    done, t_start, step = 0, time.perf_counter(), 1
+    blocks = 0
+    while True:
+        for i in range(L.n_layers):
+            oracle.step(L.fmt, L.numpy_views(i, arrs[i]), oracle.hparams(step=step, **hp_kw), threads=threads)
+            done += L.block(i)[1]
+            blocks += 1
+            if time.perf_counter() - t_start >= budget_s:
+                el = time.perf_counter() - t_start
+                return done / el, done, el, blocks
+        step += 1
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    """The oracle alone, on the host cores: each step a bounded sample of the
+    workload (whole blocks, as many as fit the per-step time budget)."""
+    import numpy as np
+    import oracle
+    import synth
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    L = build_layout(args.workload, args.max_blocks)
+    hp_kw = HP_LORA if L.fmt == "L16F" else HP
+    threads = os.cpu_count() or 1
+    # state for the sample: blocks from the start of the model
+    arrs, blocks, budget_params = [], [], None
+    # size the sample so one step takes about --ref-step-s seconds
+    i = 0
+    while i < L.n_layers:
+        a = np.empty(L.block_bytes(i), np.uint8)
+        synth.fill_block(L.numpy_views(i, a), L.spans(i), i, args.workload, L.fmt, t=1, seed=args.seed)
+        t0 = time.perf_counter()
+        oracle.step(L.fmt, L.numpy_views(i, a), oracle.hparams(step=1, **hp_kw), threads=threads)
+        dt = time.perf_counter() - t0
+        arrs.append(a)
+        blocks.append(i)
+        i += 1
+        total_est = dt * len(blocks)
+        if total_est >= args.ref_step_s:
+            break
+    sample_params = sum(L.block(b)[1] for b in blocks)
+    for w in range(args.warmup):
+        for k, b in enumerate(blocks):
+            oracle.step(L.fmt, L.numpy_views(b, arrs[k]), oracle.hparams(step=2 + w, **hp_kw), threads=threads)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        for k, b in enumerate(blocks):
+            oracle.step(L.fmt, L.numpy_views(b, arrs[k]),
+                        oracle.hparams(step=2 + args.warmup + s, **hp_kw), threads=threads)
+    el = time.perf_counter() - t0
+    value = sample_params * args.steps / el
+    sample = (f"blocks {blocks[0]}..{blocks[-1]} of {L.n_layers} ({sample_params} of {L.n_params} params) "
+              f"per step, oracle on {threads} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_for(L, args.workload, world, args.max_blocks),
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_for(L, workload, world, max_blocks=0):
+    desc = WORKLOADS[workload][2]
+    if max_blocks > 0:
+        desc += f", first {L.n_layers} blocks only"
+    return {"workload": desc, "name": workload, "layout": L.fmt, "params": L.n_params,
+            "blocks": L.n_layers, "state_bytes": sum(L.block_bytes(i) for i in range(L.n_layers)),
+            "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
+            "hparams": HP_LORA if L.fmt == "L16F" else HP}
+
+
+def link_bandwidth(torch, host_ptr_arrs, dev_a, dev_b, nbytes: int, reps: int = 5):
+    """Pinned host <-> device copy bandwidth: H2D alone, D2H alone, both at once
+    (each direction timed on its own stream with CUDA events)."""
+    h_in = torch.from_numpy(host_ptr_arrs[0][:nbytes])
+    h_out = torch.from_numpy(host_ptr_arrs[1][:nbytes])
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(h2d: bool, d2h: bool):
+        best = [float("inf"), float("inf")]
+        for _ in range(reps):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            torch.cuda.synchronize()
+            if h2d:
+                e[0].record(s1)
+                with torch.cuda.stream(s1):
+                    dev_a[:nbytes].copy_(h_in, non_blocking=True)
+                e[1].record(s1)
+            if d2h:
+                e[2].record(s2)
+                with torch.cuda.stream(s2):
+                    h_out.copy_(dev_b[:nbytes], non_blocking=True)
+                e[3].record(s2)
+            torch.cuda.synchronize()
+            if h2d:
+                best[0] = min(best[0], e[0].elapsed_time(e[1]) / 1e3)
+            if d2h:
+                best[1] = min(best[1], e[2].elapsed_time(e[3]) / 1e3)
+        return [nbytes / t / 1e9 if t < float("inf") else None for t in best]
+
+    h2d_alone, _ = timed(True, False)
+    _, d2h_alone = timed(False, True)
+    h2d_conc, d2h_conc = timed(True, True)
+    return {"h2d_gbs": h2d_alone, "d2h_gbs": d2h_alone, "h2d_concurrent_gbs": h2d_conc,
+            "d2h_concurrent_gbs": d2h_conc, "bytes": nbytes}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    from optimizer_update_gb300 import lst
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init("nccl")
+    seed = replica_seed(args.seed, rank)
+
+    L = build_layout(args.workload, args.max_blocks)
+    hp_kw = HP_LORA if L.fmt == "L16F" else HP
+    P = L.n_params
+    chunk = 1 << 22
+    L.set_stream_chunk(chunk)
+    ptrs, arrs = alloc_pinned_state(L, args.workload, seed)
+
+    # ---- device-resident leg -------------------------------------------------
+    dev = []
+    for i in range(L.n_layers):
+        d = torch.empty(L.block_bytes(i), dtype=torch.uint8, device=device)
+        d.copy_(torch.from_numpy(arrs[i]), non_blocking=False)
+        dev.append(d)
+    dptrs = [d.data_ptr() for d in dev]
+    stream = torch.cuda.Stream(device=device)
+    t = 1
+    for _ in range(args.warmup):
+        lst.lst_adamw_step(L.handle, dptrs, lst.adamw_hparams(step=t, **hp_kw), stream.cuda_stream)
+        t += 1
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    clocks = ClockSampler(vis[local] if local < len(vis) else str(local))
+    clocks.start()
+    time.sleep(0.3)
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    torch.cuda.synchronize(device)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    events[0].record(stream)
+    for k in range(args.steps):
+        lst.lst_adamw_step(L.handle, dptrs, lst.adamw_hparams(step=t, **hp_kw), stream.cuda_stream)
+        t += 1
+        events[k + 1].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    per_launch = [events[k].elapsed_time(events[k + 1]) / 1e3 for k in range(args.steps)]
+    t_dev = sum(per_launch)
+    t_dev_max = max_over_ranks(t_dev, device)
+    value = world * P * args.steps / t_dev_max
+    avg_launch = t_dev / args.steps
+    alg_bytes = ALG_BYTES[L.fmt] * P
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / avg_launch / 1e9
+    traffic = kernel_traffic(P)
+    del dev
+    torch.cuda.empty_cache()
+
+    # ---- host link, measured in this run -------------------------------------
+    buf0 = torch.empty(L.max_block_bytes, dtype=torch.uint8, device=device)
+    buf1 = torch.empty(L.max_block_bytes, dtype=torch.uint8, device=device)
+    big = [i for i in range(L.n_layers) if L.block_bytes(i) >= min(1 << 30, L.max_block_bytes)]
+    a0 = arrs[big[0]] if big else arrs[0]
+    a1 = arrs[big[-1]] if len(big) > 1 else arrs[-1]
+    nb = min(a0.size, a1.size, buf0.numel(), 1 << 30)
+    link = link_bandwidth(torch, [a0, a1], buf0, buf1, nb)
+
+    # ---- streamed leg (the public end-to-end call) ------------------------------
+    h2d_b = sum(L.transfer(i)[1] for i in range(L.n_layers))
+    d2h_b = sum(L.transfer(i)[3] for i in range(L.n_layers))
+    for _ in range(max(1, min(args.warmup, 2))):
+        lst.lst_stream_step(L.handle, ptrs, buf0.data_ptr(), buf1.data_ptr(),
+                            lst.adamw_hparams(step=t, **hp_kw), 600_000)
+        t += 1
+    e_steps = max(1, min(args.steps, args.e2e_steps))
+    barrier(device)
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        lst.lst_stream_step(L.handle, ptrs, buf0.data_ptr(), buf1.data_ptr(),
+                            lst.adamw_hparams(step=t, **hp_kw), 600_000)
+        t += 1
+    t_e2e = time.perf_counter() - t0
+    t_e2e_max = max_over_ranks(t_e2e, device)
+    e2e_value = world * P * e_steps / t_e2e_max
+    chunks = sum((L.padded(i) + chunk - 1) // chunk for i in range(L.n_layers))
+    roof_t = max(h2d_b / (link["h2d_concurrent_gbs"] * 1e9), d2h_b / (link["d2h_concurrent_gbs"] * 1e9))
+    stream_info = dict(link, step_ms=1e3 * t_e2e / e_steps,
+                       achieved_h2d_gbs=h2d_b * e_steps / t_e2e / 1e9,
+                       achieved_d2h_gbs=d2h_b * e_steps / t_e2e / 1e9,
+                       roofline_ms=1e3 * roof_t, frac_of_link_roofline=roof_t / (t_e2e / e_steps),
+                       chunk_elems=chunk)
+
+    # ---- CPU baseline: the oracle on the host cores, bounded sample ------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        rate, done, el, nblocks = cpu_oracle_rate(L, arrs, hp_kw, args.cpu_budget_s, threads)
+        cpu = {"value": rate, "unit": "params/s", "cores": threads, "kind": "oracle",
+               "sample": f"{nblocks} block updates ({done} params) of this workload's state in {el:.1f} s"}
+
+    for p in ptrs:
+        lst.lst_host_free(p)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_dev_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_for(L, args.workload, world, args.max_blocks),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": f"lst_update_kernel<{L.fmt}>", "alg_bytes_per_launch": alg_bytes,
+                         "avg_launch_ms": 1e3 * avg_launch, "peak_source": f"{peak_kind} hbm_gbs"},
+            "e2e": {"value": e2e_value, "unit": "params/s", "h2d_bytes_per_step": h2d_b,
+                    "d2h_bytes_per_step": d2h_b, "steps": e_steps, "call": "lst_stream_step",
+                    "gpu_launches": e_steps * chunks},
+            "stream": stream_info,
+            "cpu_baseline": cpu,
+            "clocks": clk,
+            "gpu_launches": args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="tinyllama_full_l16m")
+    ap.add_argument("--seed", type=int, default=0x5EED)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--ref-step-s", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--max-blocks", type=int, default=0,
+                    help="keep only the first N blocks of the workload (a smaller case)")
+    args = ap.parse_args(argv)
+    # at least three untimed warm-up steps, whatever is asked; the line reports
+    # the number actually run
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

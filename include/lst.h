@@ -1,0 +1,245 @@
+/*
+ * lst.h - layer-streamed optimizer update over packed per-layer state blocks.
+ *
+ * C ABI of liblst.so (GB300, sm_103a). Plain pointers and sizes only.
+ *
+ * The method. Training state (weights W, gradients G, Adam moments m, v and,
+ * in one layout, an fp32 master copy of W) lives in one contiguous block per
+ * transformer layer. The optimizer updates each block with the per-parameter
+ * Adam rule written as an additive delta on the stored weight
+ *   m' = b1*m + (1-b1)*g,  v' = b2*v + (1-b2)*g^2,
+ *   m^ = m'/(1-b1^t),      v^ = v'/(1-b2^t),
+ *   W += -(lr * m^/(sqrt(v^) + eps))           (t: one global step counter)
+ * ("Training 70B Models on Consumer Hardware (If You're Willing to Wait)",
+ * section "The Math"), or with the SGD form W += (-lr*g) (same page, section
+ * "The Assumption Everyone Makes"). Blocks are either resident in device
+ * memory, or held in pinned host memory and streamed through the device one
+ * layer at a time over two device buffers and three CUDA streams ordered by
+ * events ("MegaTrain" summary page, sections on layer-contiguous memory
+ * tiling, the double-buffered pipeline and three-stream execution).
+ *
+ * Arithmetic (both the device-resident and the streamed path compute exactly
+ * this, so their results are bit-identical):
+ *   - every step below is one IEEE fp32 operation, rounded to nearest, in this
+ *     order, with no fused multiply-add:
+ *       m = b1*m + omb1*g;  v = b2*v + omb2*(g*g);
+ *       mh = m/bc1;  vh = v/bc2;  u = mh/(sqrt(vh) + eps);
+ *       w = w*decay - lr*u
+ *   - omb1 = 1-b1, omb2 = 1-b2, bc1 = 1-b1^t, bc2 = 1-b2^t and
+ *     decay = 1 - lr*weight_decay are formed in double on the host and rounded
+ *     once to fp32. Weight decay is decoupled (AdamW) and applied to the weight
+ *     before the Adam step; the pages themselves give plain Adam.
+ *   - bf16 values are widened exactly; bf16 results are the fp32 result
+ *     rounded to nearest, ties to even.
+ *   - SGD: w = w + (-(lr*g)); m and v are not touched, no decay.
+ *
+ * Layouts (per parameter; a block is segment-of-arrays, one segment per field,
+ * in the order listed, each segment starting on a 4 KB boundary):
+ *   LST_L12_BF16   G bf16 | W bf16 | m f32 | v f32                 12 B
+ *   LST_L16_MIXED  G bf16 | master f32 | m f32 | v f32 | W bf16    16 B
+ *                  (W is an output: the new master rounded to bf16)
+ *   LST_L16_FP32   G f32 | W f32 | m f32 | v f32                   16 B
+ * Within a block, tensors follow in the order given to lst_layout_create, each
+ * starting at an element index that is a multiple of 8; the block's element
+ * count is rounded up to a multiple of 2048. Padding elements must hold zero:
+ * the update maps a zero element (g = W = m = v = 0) to zero, and the kernels
+ * update padding along with the tensors.
+ * G comes first and the output fields last, so the bytes sent host -> device
+ * (the fields the update reads) are one prefix of the block, and the bytes
+ * sent back (the fields it writes) are one suffix.
+ *
+ * Ownership: the caller owns all host and device memory and keeps it valid
+ * for the duration of a call (and, for the asynchronous lst_adamw_step /
+ * lst_sgd_step, until the work on the given stream has finished). The layout
+ * handle is owned by the library and freed with lst_layout_destroy. The step
+ * calls allocate no device memory.
+ *
+ * Errors: every call returns an lst_status and never aborts or exits. On
+ * LST_ERR_CUDA the CUDA error text is available from lst_last_error() (per
+ * thread). A call that fails validation touches no memory.
+ *
+ * Threads: a layout may be used from several threads for lst_adamw_step /
+ * lst_sgd_step. lst_stream_step serialises itself per layout.
+ */
+#ifndef LST_H
+#define LST_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LST_API __attribute__((visibility("default")))
+#else
+#define LST_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum lst_status {
+  LST_OK = 0,
+  LST_ERR_INVALID_ARG = 1, /* null pointer, bad size, hyperparameter outside its domain */
+  LST_ERR_ALIGNMENT = 2,   /* pointer not aligned as the call requires */
+  LST_ERR_NOT_PINNED = 3,  /* host block not page-locked (pinned) host memory */
+  LST_ERR_CUDA = 4,        /* a CUDA runtime call failed; see lst_last_error() */
+  LST_ERR_OOM = 5,         /* host allocation failed */
+  LST_ERR_TIMEOUT = 6      /* lst_stream_step's host-side deadline passed */
+} lst_status;
+
+typedef enum lst_format {
+  LST_L12_BF16 = 0,  /* 12 B/param: bf16 W, bf16 G, fp32 m, v */
+  LST_L16_MIXED = 1, /* 16 B/param: 12 B + fp32 master, bf16 W derived */
+  LST_L16_FP32 = 2   /* 16 B/param: fp32 W, G, m, v */
+} lst_format;
+
+typedef enum lst_field {
+  LST_FIELD_G = 0,
+  LST_FIELD_W = 1,
+  LST_FIELD_M = 2,
+  LST_FIELD_V = 3,
+  LST_FIELD_MASTER = 4 /* LST_L16_MIXED only */
+} lst_field;
+
+typedef struct lst_layout lst_layout; /* opaque, owned by the library */
+
+/* AdamW hyperparameters. step = t >= 1, the global step counter ("The Math":
+   one scalar t for all layers, incremented each batch). 0 <= beta < 1;
+   lr, eps, weight_decay finite. */
+typedef struct lst_adamw_hparams {
+  float lr, beta1, beta2, eps, weight_decay;
+  int64_t step;
+} lst_adamw_hparams;
+
+/* ------------------------------------------------------------------------
+ * Block geometry ("MegaTrain" summary page, layer-contiguous memory tiling:
+ * one contiguous, 4 KB-aligned block per transformer layer). Host only.
+ * ------------------------------------------------------------------------ */
+
+/* Build a layout from n_tensors tensor shapes.
+   ndim[i] in 0..4; dims holds 4 entries per tensor (dims[4*i + k], entries
+   beyond ndim[i] ignored; a dimension of 0 gives an empty tensor).
+   layer_of_tensor[i] is the block the tensor belongs to; blocks are numbered
+   0..L-1 and each must hold at least one tensor. n_tensors == 0 gives a
+   layout with no blocks. The arrays are read during the call only.
+   Errors: LST_ERR_INVALID_ARG (null pointers with n_tensors > 0, ndim out of
+   range, negative dims, a block index < 0 or a block without tensors, a
+   block larger than 2^40 elements, unknown format), LST_ERR_OOM. */
+LST_API lst_status lst_layout_create(int32_t n_tensors, const int32_t* ndim, const int64_t* dims,
+                             const int32_t* layer_of_tensor, lst_format fmt, lst_layout** out);
+
+/* Free a layout (null is ignored). Not concurrently with a call using it. */
+LST_API void lst_layout_destroy(lst_layout* layout);
+
+/* Number of blocks, total parameters (without padding), and the largest
+   block's size in bytes. Any output pointer may be null. */
+LST_API lst_status lst_layout_info(const lst_layout* layout, int64_t* n_layers, int64_t* n_params,
+                           int64_t* max_block_bytes);
+
+/* One block: its size in bytes, its parameter count (no padding) and its
+   padded element count (the length of each segment in elements). Outputs may
+   be null. LST_ERR_INVALID_ARG if layer is out of range. */
+LST_API lst_status lst_layout_block(const lst_layout* layout, int64_t layer, int64_t* bytes, int64_t* params,
+                            int64_t* padded_elems);
+
+/* Byte offset and size of one field's segment within a block.
+   LST_ERR_INVALID_ARG if the field does not exist in the layout's format. */
+LST_API lst_status lst_layout_segment(const lst_layout* layout, int64_t layer, int32_t field,
+                              int64_t* byte_offset, int64_t* bytes);
+
+/* Byte offset, within its block, of a tensor's data in one field's segment
+   (for building views of the block), and the tensor's block and element
+   offset (either output may be null). */
+LST_API lst_status lst_layout_tensor(const lst_layout* layout, int32_t tensor, int32_t field,
+                             int64_t* byte_offset, int64_t* layer, int64_t* elem_offset);
+
+/* The contiguous byte ranges of a block that the streamed step sends to the
+   device (the fields the update reads) and copies back (the fields it
+   writes). The gradient is never copied back. */
+LST_API lst_status lst_layout_transfer(const lst_layout* layout, int64_t layer, int64_t* h2d_offset,
+                               int64_t* h2d_bytes, int64_t* d2h_offset, int64_t* d2h_bytes);
+
+/* Element count of the sub-chunks the streamed step moves and updates at a
+   time (a multiple of 2048; 0 = one chunk per block). Default 4,194,304. */
+LST_API lst_status lst_layout_set_stream_chunk(lst_layout* layout, int64_t elems);
+
+/* ------------------------------------------------------------------------
+ * Device-resident step.
+ * ------------------------------------------------------------------------ */
+
+/* One AdamW step over every block, all blocks resident in device memory.
+   dev_blocks: n_layers device pointers, one per block, each 16-byte aligned
+   (null allowed only for a zero-byte block); the array itself is host memory
+   and is read during the call only.
+   cuda_stream: a cudaStream_t (null = the legacy default stream). The call
+   enqueues one kernel launch per 128 blocks on that stream and returns; the
+   update is complete when the stream reaches that point.
+   Errors: LST_ERR_INVALID_ARG (null layout/hparams/dev_blocks, hparams outside
+   their domain), LST_ERR_ALIGNMENT, LST_ERR_CUDA (launch failure). Validation
+   happens before any CUDA call. */
+LST_API lst_status lst_adamw_step(const lst_layout* layout, void* const* dev_blocks,
+                          const lst_adamw_hparams* hparams, void* cuda_stream);
+
+/* One SGD step, W += (-lr*g), over every block (m and v untouched; in the
+   mixed layout the master moves and W is re-derived). As lst_adamw_step. */
+LST_API lst_status lst_sgd_step(const lst_layout* layout, void* const* dev_blocks, float lr,
+                        void* cuda_stream);
+
+/* ------------------------------------------------------------------------
+ * Streamed step ("MegaTrain" summary page: host memory is the authoritative
+ * store; StreamIn over a weight stream, compute, offload over a second copy
+ * stream; two buffers ping-pong; events weights-ready, update-done and
+ * buffer-free; no host-side barrier).
+ * ------------------------------------------------------------------------ */
+
+/* One AdamW step over every block, blocks in pinned host memory.
+   host_blocks: n_layers pointers to page-locked host memory (cudaHostAlloc,
+   cudaHostRegister or lst_host_alloc), each 4096-byte aligned and at least
+   the block's size. dev_buf0, dev_buf1: two device buffers, each 256-byte
+   aligned and at least max_block_bytes (lst_layout_info) long; block i is
+   staged in buffer i & 1, at the block's own offsets.
+   For each block, in sub-chunks of the layout's stream chunk size: the input
+   prefix is copied host -> device on a copy stream, the update runs on a
+   compute stream, and the output suffix is copied device -> host on a second
+   copy stream; the streams wait only on events. Results are bit-identical to
+   lst_adamw_step on the same data.
+   Synchronous: returns when all copies back to the host blocks are complete,
+   or with LST_ERR_TIMEOUT once timeout_ms has passed (timeout_ms <= 0: no
+   deadline); in that case work
+   may still be in flight and the caller must synchronize the device before
+   touching or freeing host_blocks or the device buffers. The device buffers
+   must not be in use by other work during the call.
+   Errors: LST_ERR_INVALID_ARG, LST_ERR_ALIGNMENT, LST_ERR_NOT_PINNED,
+   LST_ERR_CUDA (after draining what was already enqueued; blocks before the
+   failure point may already hold updated state, so the step must be treated
+   as failed as a whole), LST_ERR_TIMEOUT. */
+LST_API lst_status lst_stream_step(const lst_layout* layout, void* const* host_blocks, void* dev_buf0,
+                           void* dev_buf1, const lst_adamw_hparams* hparams, int64_t timeout_ms);
+
+/* ------------------------------------------------------------------------
+ * Utilities.
+ * ------------------------------------------------------------------------ */
+
+/* Page-locked host memory (cudaHostAlloc), page aligned. Free with
+   lst_host_free. */
+LST_API lst_status lst_host_alloc(int64_t bytes, void** out);
+LST_API lst_status lst_host_free(void* ptr);
+
+/* Static description of a status code. */
+LST_API const char* lst_status_string(lst_status status);
+
+/* Text of the last error raised on the calling thread ("" if none). */
+LST_API const char* lst_last_error(void);
+
+/* Test hook (host-side fault injection; no device fault is ever caused).
+   kind 0: clear. kind 1: the k-th asynchronous enqueue (copy, launch, event
+   record or wait; counted from 1 within each later lst_stream_step call)
+   reports a failure instead of being issued. kind 2: lst_stream_step never
+   observes completion, so it returns LST_ERR_TIMEOUT at its deadline (after
+   which it still drains its own work before returning). */
+LST_API lst_status lst_test_inject(int32_t kind, int64_t k);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LST_H */

@@ -1,0 +1,163 @@
+// C ABI entry points of liblst: validation, step scalars, the device-resident
+// step, host pinned allocation, status text and the host-side test hook.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "lst_internal.h"
+
+namespace lst {
+
+static thread_local char g_err[512] = "";
+
+void clear_error() { g_err[0] = '\0'; }
+
+lst_status fail(lst_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+lst_status cuda_fail(cudaError_t err, const char* what) {
+  return fail(LST_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(err), cudaGetErrorName(err));
+}
+
+Inject& inject() {
+  static Inject s;
+  return s;
+}
+
+bool valid_hparams(const lst_adamw_hparams* hp) {
+  if (!hp) return false;
+  if (hp->step < 1) return false;
+  if (!(hp->beta1 >= 0.0f && hp->beta1 < 1.0f)) return false;
+  if (!(hp->beta2 >= 0.0f && hp->beta2 < 1.0f)) return false;
+  if (!std::isfinite(hp->lr) || !std::isfinite(hp->eps) || !std::isfinite(hp->weight_decay)) return false;
+  return true;
+}
+
+// Step scalars: formed in double, rounded once to fp32 ("The Math": bias
+// corrections 1 - beta^t with the global step t).
+bool make_scalars(const lst_adamw_hparams& hp, Scalars* s) {
+  if (!valid_hparams(&hp)) return false;
+  const double b1 = hp.beta1, b2 = hp.beta2, t = (double)hp.step;
+  s->beta1 = hp.beta1;
+  s->beta2 = hp.beta2;
+  s->one_minus_beta1 = (float)(1.0 - b1);
+  s->one_minus_beta2 = (float)(1.0 - b2);
+  s->bias_correction1 = (float)(1.0 - std::pow(b1, t));
+  s->bias_correction2 = (float)(1.0 - std::pow(b2, t));
+  s->eps = hp.eps;
+  s->lr = hp.lr;
+  s->decay = (float)(1.0 - (double)hp.lr * (double)hp.weight_decay);
+  return true;
+}
+
+}  // namespace lst
+
+using namespace lst;
+
+static lst_status device_step(const lst_layout* L, void* const* dev_blocks, const Scalars& s, bool sgd,
+                              void* cuda_stream, const char* who) {
+  const int64_t n = (int64_t)L->blocks.size();
+  if (n == 0) return LST_OK;
+  if (!dev_blocks) return fail(LST_ERR_INVALID_ARG, "%s: dev_blocks is null", who);
+  for (int64_t i = 0; i < n; ++i) {
+    const Block& b = L->blocks[(size_t)i];
+    if (b.bytes == 0) continue;
+    if (!dev_blocks[i]) return fail(LST_ERR_INVALID_ARG, "%s: block %lld pointer is null", who, (long long)i);
+    if (reinterpret_cast<uintptr_t>(dev_blocks[i]) % 16 != 0)
+      return fail(LST_ERR_ALIGNMENT, "%s: block %lld pointer not 16-byte aligned", who, (long long)i);
+  }
+  std::vector<Run> runs;
+  try {
+    runs.reserve((size_t)n);
+  } catch (...) {
+    return fail(LST_ERR_OOM, "%s: out of host memory", who);
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    const Block& b = L->blocks[(size_t)i];
+    if (b.padded == 0) continue;
+    runs.push_back(block_run(*L, b, static_cast<char*>(dev_blocks[i]), 0, b.padded));
+  }
+  cudaError_t err = launch_update(L->fmt, sgd, runs.data(), (int)runs.size(), s,
+                                  static_cast<cudaStream_t>(cuda_stream));
+  if (err != cudaSuccess) return cuda_fail(err, who);
+  return LST_OK;
+}
+
+extern "C" lst_status lst_adamw_step(const lst_layout* L, void* const* dev_blocks,
+                                     const lst_adamw_hparams* hp, void* cuda_stream) {
+  clear_error();
+  if (!L) return fail(LST_ERR_INVALID_ARG, "lst_adamw_step: null layout");
+  if (!hp) return fail(LST_ERR_INVALID_ARG, "lst_adamw_step: null hparams");
+  Scalars s;
+  if (!make_scalars(*hp, &s))
+    return fail(LST_ERR_INVALID_ARG,
+                "lst_adamw_step: hyperparameters outside their domain (step >= 1, 0 <= beta < 1, finite)");
+  return device_step(L, dev_blocks, s, false, cuda_stream, "lst_adamw_step");
+}
+
+extern "C" lst_status lst_sgd_step(const lst_layout* L, void* const* dev_blocks, float lr,
+                                   void* cuda_stream) {
+  clear_error();
+  if (!L) return fail(LST_ERR_INVALID_ARG, "lst_sgd_step: null layout");
+  if (!std::isfinite(lr)) return fail(LST_ERR_INVALID_ARG, "lst_sgd_step: lr not finite");
+  Scalars s;
+  std::memset(&s, 0, sizeof(s));
+  s.lr = lr;
+  return device_step(L, dev_blocks, s, true, cuda_stream, "lst_sgd_step");
+}
+
+extern "C" lst_status lst_host_alloc(int64_t bytes, void** out) {
+  clear_error();
+  if (!out) return fail(LST_ERR_INVALID_ARG, "lst_host_alloc: out is null");
+  *out = nullptr;
+  if (bytes <= 0) return fail(LST_ERR_INVALID_ARG, "lst_host_alloc: bytes must be > 0");
+  cudaError_t err = cudaHostAlloc(out, (size_t)bytes, cudaHostAllocDefault);
+  if (err == cudaErrorMemoryAllocation) {
+    cudaGetLastError();
+    *out = nullptr;
+    return fail(LST_ERR_OOM, "lst_host_alloc: %lld bytes: out of pinned host memory", (long long)bytes);
+  }
+  if (err != cudaSuccess) {
+    *out = nullptr;
+    return cuda_fail(err, "lst_host_alloc");
+  }
+  return LST_OK;
+}
+
+extern "C" lst_status lst_host_free(void* p) {
+  clear_error();
+  if (!p) return LST_OK;
+  cudaError_t err = cudaFreeHost(p);
+  if (err != cudaSuccess) return cuda_fail(err, "lst_host_free");
+  return LST_OK;
+}
+
+extern "C" const char* lst_status_string(lst_status st) {
+  switch (st) {
+    case LST_OK: return "ok";
+    case LST_ERR_INVALID_ARG: return "invalid argument";
+    case LST_ERR_ALIGNMENT: return "misaligned pointer";
+    case LST_ERR_NOT_PINNED: return "host memory not pinned";
+    case LST_ERR_CUDA: return "CUDA error";
+    case LST_ERR_OOM: return "out of memory";
+    case LST_ERR_TIMEOUT: return "timed out";
+  }
+  return "unknown status";
+}
+
+extern "C" const char* lst_last_error(void) { return g_err; }
+
+extern "C" lst_status lst_test_inject(int32_t kind, int64_t k) {
+  clear_error();
+  if (kind < 0 || kind > 2) return fail(LST_ERR_INVALID_ARG, "lst_test_inject: unknown kind %d", kind);
+  if (kind == 1 && k < 1) return fail(LST_ERR_INVALID_ARG, "lst_test_inject: k must be >= 1");
+  inject().k.store(k);
+  inject().kind.store(kind);
+  return LST_OK;
+}

@@ -1,0 +1,112 @@
+// Internal declarations shared by liblst's translation units (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/lst.h"
+
+namespace lst {
+
+constexpr int kMaxFields = 5;
+constexpr int64_t kTensorAlign = 8;     // elements: 16 B in a bf16 segment
+constexpr int64_t kBlockAlign = 2048;   // elements: every segment a whole number of 4 KB pages
+constexpr int64_t kWarpSpan = 256;      // elements one warp covers per task (kernel tiling)
+constexpr int64_t kMaxBlockElems = int64_t(1) << 40;
+constexpr int64_t kDefaultStreamChunk = int64_t(1) << 22;
+
+// Segment order and element size of each format.
+struct FormatInfo {
+  int n_segments;
+  int field[kMaxFields];      // field id of segment k
+  int elem_bytes[kMaxFields]; // element size of segment k
+  int n_inputs;               // segments [0, n_inputs) are read by the update
+  int first_output;           // segments [first_output, n_segments) are written
+  int bytes_per_param;
+};
+const FormatInfo& format_info(lst_format fmt);
+
+struct Block {
+  int64_t params = 0;    // sum of tensor sizes
+  int64_t padded = 0;    // elements per segment
+  int64_t bytes = 0;
+  int64_t seg_off[kMaxFields];    // by field id, -1 if absent
+  int64_t h2d_off = 0, h2d_bytes = 0, d2h_off = 0, d2h_bytes = 0;
+};
+
+struct Tensor {
+  int64_t layer = 0;
+  int64_t elem_off = 0;
+  int64_t numel = 0;
+};
+
+struct Engine;  // streamed-step resources (streams, events), per device
+
+}  // namespace lst
+
+struct lst_layout {
+  lst_format fmt;
+  int64_t n_params = 0;
+  int64_t max_block_bytes = 0;
+  int64_t stream_chunk = lst::kDefaultStreamChunk;
+  std::vector<lst::Block> blocks;
+  std::vector<lst::Tensor> tensors;
+  std::mutex stream_mu;           // serialises lst_stream_step on this layout
+  lst::Engine* engine = nullptr;  // created on first lst_stream_step
+};
+
+namespace lst {
+
+// One contiguous run of elements the update kernel walks: pointers to the
+// first element of the run in every segment it touches. `w` is the weight the
+// update reads and writes (bf16 W for L12, fp32 master for L16M, fp32 W for
+// L16F); `w16` is the bf16 W written from the master (L16M only).
+struct Run {
+  const void* g;
+  void* w;
+  float* m;
+  float* v;
+  void* w16;
+  int64_t elems;  // multiple of kWarpSpan
+};
+
+// fp32 step scalars, formed in double on the host and rounded once.
+struct Scalars {
+  float beta1, beta2, one_minus_beta1, one_minus_beta2;
+  float bias_correction1, bias_correction2;
+  float eps, lr, decay;
+};
+
+bool make_scalars(const lst_adamw_hparams& hp, Scalars* s);
+bool valid_hparams(const lst_adamw_hparams* hp);
+
+// Build the run of block `b` whose base address is `base`, covering elements
+// [e0, e1) of every segment.
+Run block_run(const lst_layout& L, const Block& b, char* base, int64_t e0, int64_t e1);
+
+// Enqueue the update over `runs` on `stream` (one launch per kMaxRunsPerLaunch
+// runs). Returns the first CUDA error, cudaSuccess otherwise.
+cudaError_t launch_update(lst_format fmt, bool sgd, const Run* runs, int n_runs, const Scalars& s,
+                          cudaStream_t stream);
+constexpr int kMaxRunsPerLaunch = 128;
+
+// Error reporting (thread-local text).
+lst_status fail(lst_status st, const char* fmt, ...);
+lst_status cuda_fail(cudaError_t err, const char* what);
+void clear_error();
+
+// Fault-injection hook state (test only).
+struct Inject {
+  std::atomic<int> kind{0};
+  std::atomic<int64_t> k{0};
+};
+Inject& inject();
+
+void destroy_engine(Engine* e);
+
+}  // namespace lst

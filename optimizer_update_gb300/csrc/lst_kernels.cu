@@ -1,0 +1,243 @@
+// Fused per-parameter AdamW / SGD update over packed per-layer state blocks.
+//
+// The arithmetic is the Adam rule written as an additive delta on the stored
+// weight ("Training 70B Models on Consumer Hardware (If You're Willing to
+// Wait)", section "The Math"), with decoupled weight decay applied to the
+// pre-step weight, and the SGD form W += (-lr*g) (same page, section "The
+// Assumption Everyone Makes"). Every step is one IEEE fp32 operation with
+// round-to-nearest (explicit _rn intrinsics, so no multiply-add contraction),
+// in the order stated in include/lst.h.
+//
+// Design (GB300, sm_103a). The update is elementwise and moves 22-28 bytes per
+// parameter for ~15 flops, so it is bound by HBM bandwidth, not by tensor
+// cores or ALUs. The kernel therefore:
+//   * walks every segment with fully coalesced vector accesses: a warp covers
+//     256 consecutive elements per task; lane k owns elements 4k..4k+3 and
+//     128+4k..128+4k+3, so each warp-wide access is one contiguous 256 B
+//     (bf16) or 512 B (fp32) range;
+//   * is persistent and grid-strided: the grid is sized to fill every SM at
+//     the occupancy the compiler allows, and tasks of all runs (blocks or
+//     sub-chunks of blocks) are dealt round-robin over all warps from one
+//     global task index, so many small runs (e.g. 308 LoRA tensors in 22
+//     blocks) load-balance like one large one;
+//   * keeps both quads of a task in flight before computing, and uses
+//     streaming (evict-first) loads and stores: every byte is touched once.
+// The run table travels in the kernel's parameter space (__grid_constant__),
+// so a step needs no device-side scratch memory and no host-to-device copy of
+// metadata.
+#include <cuda_bf16.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "lst_internal.h"
+
+namespace lst {
+
+struct RunTable {
+  int32_t n;
+  int32_t pad_;
+  struct Entry {
+    const void* g;
+    void* w;
+    float* m;
+    float* v;
+    void* w16;
+    long long tasks;       // elements / 256
+    long long first_task;  // global index of this run's first task in the launch
+  } r[kMaxRunsPerLaunch];
+};
+static_assert(sizeof(RunTable) < 30000, "kernel parameter space");
+
+// ---- element math ---------------------------------------------------------
+
+__device__ __forceinline__ float adamw_elem(float g, float w, float& m, float& v, const Scalars& s) {
+  const float m_new = __fadd_rn(__fmul_rn(s.beta1, m), __fmul_rn(s.one_minus_beta1, g));
+  const float v_new = __fadd_rn(__fmul_rn(s.beta2, v), __fmul_rn(s.one_minus_beta2, __fmul_rn(g, g)));
+  m = m_new;
+  v = v_new;
+  const float m_hat = __fdiv_rn(m_new, s.bias_correction1);
+  const float v_hat = __fdiv_rn(v_new, s.bias_correction2);
+  const float u = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), s.eps));
+  return __fsub_rn(__fmul_rn(w, s.decay), __fmul_rn(s.lr, u));
+}
+
+__device__ __forceinline__ float sgd_elem(float g, float w, float lr) {
+  return __fadd_rn(w, -__fmul_rn(lr, g));
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// Two fp32 values -> two bf16 (round to nearest even), low half = first.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---- one quad (4 consecutive elements) per format --------------------------
+
+enum { F_L12 = 0, F_L16M = 1, F_L16F = 2 };
+
+template <int FMT, bool SGD>
+struct Quad {
+  float4 g, w, m, v;
+};
+
+template <int FMT, bool SGD>
+__device__ __forceinline__ void load_quad(const RunTable::Entry& R, long long e, Quad<FMT, SGD>& q) {
+  if (FMT == F_L16F) {
+    q.g = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(R.g) + e));
+    q.w = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(R.w) + e));
+  } else {
+    const uint2 gb = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(R.g) + e));
+    q.g = make_float4(bf16_lo(gb.x), bf16_hi(gb.x), bf16_lo(gb.y), bf16_hi(gb.y));
+    if (FMT == F_L12) {
+      const uint2 wb = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(R.w) + e));
+      q.w = make_float4(bf16_lo(wb.x), bf16_hi(wb.x), bf16_lo(wb.y), bf16_hi(wb.y));
+    } else {
+      q.w = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(R.w) + e));
+    }
+  }
+  if (!SGD) {
+    q.m = __ldcs(reinterpret_cast<const float4*>(R.m + e));
+    q.v = __ldcs(reinterpret_cast<const float4*>(R.v + e));
+  }
+}
+
+template <int FMT, bool SGD>
+__device__ __forceinline__ void update_store_quad(const RunTable::Entry& R, long long e, Quad<FMT, SGD>& q,
+                                                  const Scalars& s) {
+  float4 w;
+  if (SGD) {
+    w.x = sgd_elem(q.g.x, q.w.x, s.lr);
+    w.y = sgd_elem(q.g.y, q.w.y, s.lr);
+    w.z = sgd_elem(q.g.z, q.w.z, s.lr);
+    w.w = sgd_elem(q.g.w, q.w.w, s.lr);
+  } else {
+    w.x = adamw_elem(q.g.x, q.w.x, q.m.x, q.v.x, s);
+    w.y = adamw_elem(q.g.y, q.w.y, q.m.y, q.v.y, s);
+    w.z = adamw_elem(q.g.z, q.w.z, q.m.z, q.v.z, s);
+    w.w = adamw_elem(q.g.w, q.w.w, q.m.w, q.v.w, s);
+    __stcs(reinterpret_cast<float4*>(R.m + e), q.m);
+    __stcs(reinterpret_cast<float4*>(R.v + e), q.v);
+  }
+  if (FMT == F_L12) {
+    uint2 wb = make_uint2(pack_bf16x2(w.x, w.y), pack_bf16x2(w.z, w.w));
+    __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(R.w) + e), wb);
+  } else {
+    __stcs(reinterpret_cast<float4*>(static_cast<float*>(R.w) + e), w);
+    if (FMT == F_L16M) {
+      uint2 wb = make_uint2(pack_bf16x2(w.x, w.y), pack_bf16x2(w.z, w.w));
+      __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(R.w16) + e), wb);
+    }
+  }
+}
+
+// ---- the kernel -------------------------------------------------------------
+
+constexpr int kThreads = 256;
+
+template <int FMT, bool SGD>
+__global__ void __launch_bounds__(kThreads) lst_update_kernel(const __grid_constant__ RunTable tab,
+                                                              const Scalars s) {
+  const int lane = threadIdx.x & 31;
+  const long long n_warps = (long long)gridDim.x * (kThreads / 32);
+  const long long warp = (long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  for (int r = 0; r < tab.n; ++r) {
+    const RunTable::Entry& R = tab.r[r];
+    // Task j of this run is global task first_task + j, owned by warp
+    // (first_task + j) mod n_warps.
+    long long j = (warp - R.first_task) % n_warps;
+    if (j < 0) j += n_warps;
+    for (; j < R.tasks; j += n_warps) {
+      const long long e = j * 256 + lane * 4;
+      Quad<FMT, SGD> a, b;
+      load_quad<FMT, SGD>(R, e, a);
+      load_quad<FMT, SGD>(R, e + 128, b);
+      update_store_quad<FMT, SGD>(R, e, a, s);
+      update_store_quad<FMT, SGD>(R, e + 128, b, s);
+    }
+  }
+}
+
+// ---- launch -----------------------------------------------------------------
+
+typedef void (*KernelFn)(const RunTable, const Scalars);
+
+static KernelFn kernel_for(lst_format fmt, bool sgd) {
+  switch (fmt) {
+    case LST_L12_BF16: return sgd ? lst_update_kernel<F_L12, true> : lst_update_kernel<F_L12, false>;
+    case LST_L16_MIXED: return sgd ? lst_update_kernel<F_L16M, true> : lst_update_kernel<F_L16M, false>;
+    default: return sgd ? lst_update_kernel<F_L16F, true> : lst_update_kernel<F_L16F, false>;
+  }
+}
+
+// Resident CTAs per SM for each kernel instantiation, and SM count, per device.
+struct DeviceInfo {
+  int sms = 0;
+  int ctas_per_sm[6] = {0, 0, 0, 0, 0, 0};
+};
+constexpr int kMaxDevices = 64;
+static DeviceInfo g_dev[kMaxDevices];
+static std::mutex g_dev_mu;
+
+static cudaError_t resident_ctas(lst_format fmt, bool sgd, int* total) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const int slot = (int)fmt * 2 + (sgd ? 1 : 0);
+  std::lock_guard<std::mutex> g(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.sms == 0) {
+    err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+  }
+  if (d.ctas_per_sm[slot] == 0) {
+    int n = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_for(fmt, sgd), kThreads, 0);
+    if (err != cudaSuccess) return err;
+    d.ctas_per_sm[slot] = n > 0 ? n : 1;
+  }
+  *total = d.sms * d.ctas_per_sm[slot];
+  return cudaSuccess;
+}
+
+cudaError_t launch_update(lst_format fmt, bool sgd, const Run* runs, int n_runs, const Scalars& s,
+                          cudaStream_t stream) {
+  int max_ctas = 0;
+  cudaError_t err = resident_ctas(fmt, sgd, &max_ctas);
+  if (err != cudaSuccess) return err;
+  KernelFn fn = kernel_for(fmt, sgd);
+  int i = 0;
+  while (i < n_runs) {
+    RunTable tab;
+    tab.n = 0;
+    tab.pad_ = 0;
+    long long tasks = 0;
+    for (; i < n_runs && tab.n < kMaxRunsPerLaunch; ++i) {
+      const Run& r = runs[i];
+      if (r.elems <= 0) continue;
+      RunTable::Entry& e = tab.r[tab.n++];
+      e.g = r.g;
+      e.w = r.w;
+      e.m = r.m;
+      e.v = r.v;
+      e.w16 = r.w16;
+      e.tasks = r.elems / kWarpSpan;
+      e.first_task = tasks;
+      tasks += e.tasks;
+    }
+    if (tab.n == 0) continue;
+    const long long warps_per_cta = kThreads / 32;
+    long long grid = (tasks + warps_per_cta - 1) / warps_per_cta;
+    if (grid > max_ctas) grid = max_ctas;
+    fn<<<(unsigned)grid, kThreads, 0, stream>>>(tab, s);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace lst

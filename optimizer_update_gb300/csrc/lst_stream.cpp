@@ -1,0 +1,299 @@
+// Streamed step: StreamIn -> update -> StreamOut over host-pinned blocks.
+//
+// "MegaTrain" summary page, sections on the double-buffered pipeline and on
+// three-stream execution: host memory holds the authoritative state; two
+// device buffers ping-pong; a weight-transfer stream copies host -> device, a
+// compute stream runs the layer, a third stream copies device -> host; the
+// streams are ordered only by events (weights ready, done, buffer free), with
+// no host-side barrier and no CUDA Graph. Here the compute is the optimizer
+// update itself, so the event that releases the outbound copy is
+// "update done".
+//
+// GB300 specifics. The host link (NVLink-C2C on Grace systems) is duplex, so
+// the inbound and outbound copies of different sub-chunks overlap. Each block
+// is moved in sub-chunks (the layout's stream chunk, default 4 Mi elements):
+// chunk c's update starts as soon as chunk c has arrived and its outbound copy
+// as soon as its update is done, so the pipeline fills and drains in one
+// sub-chunk rather than one whole block. Block i is staged in buffer i & 1 at
+// the block's own offsets; block i+2's inbound copies wait for the event that
+// block i's last outbound copy recorded. Events are re-recorded per chunk: a
+// stream wait binds to the most recent record enqueued before it, and all
+// enqueues come from this one host thread in order.
+#include <chrono>
+#include <new>
+#include <thread>
+
+#include "lst_internal.h"
+
+namespace lst {
+
+struct Engine {
+  int device = -1;
+  cudaStream_t h2d = nullptr, compute = nullptr, d2h = nullptr;
+  cudaEvent_t weights_ready[2] = {nullptr, nullptr};
+  cudaEvent_t update_done[2] = {nullptr, nullptr};
+  cudaEvent_t buffer_free[2] = {nullptr, nullptr};
+  cudaEvent_t done = nullptr;
+};
+
+static void release(Engine* e) {
+  for (int b = 0; b < 2; ++b) {
+    if (e->weights_ready[b]) cudaEventDestroy(e->weights_ready[b]);
+    if (e->update_done[b]) cudaEventDestroy(e->update_done[b]);
+    if (e->buffer_free[b]) cudaEventDestroy(e->buffer_free[b]);
+  }
+  if (e->done) cudaEventDestroy(e->done);
+  if (e->h2d) cudaStreamDestroy(e->h2d);
+  if (e->compute) cudaStreamDestroy(e->compute);
+  if (e->d2h) cudaStreamDestroy(e->d2h);
+  *e = Engine();
+}
+
+void destroy_engine(Engine* e) {
+  if (!e) return;
+  int prev = -1;
+  if (e->device >= 0 && cudaGetDevice(&prev) == cudaSuccess) {
+    cudaSetDevice(e->device);
+    release(e);
+    cudaSetDevice(prev);
+  }
+  delete e;
+}
+
+static cudaError_t create(Engine* e, int device) {
+  e->device = device;
+  cudaError_t err;
+  const unsigned f = cudaStreamNonBlocking;
+  if ((err = cudaStreamCreateWithFlags(&e->h2d, f)) != cudaSuccess) return err;
+  if ((err = cudaStreamCreateWithFlags(&e->compute, f)) != cudaSuccess) return err;
+  if ((err = cudaStreamCreateWithFlags(&e->d2h, f)) != cudaSuccess) return err;
+  const unsigned ef = cudaEventDisableTiming;
+  for (int b = 0; b < 2; ++b) {
+    if ((err = cudaEventCreateWithFlags(&e->weights_ready[b], ef)) != cudaSuccess) return err;
+    if ((err = cudaEventCreateWithFlags(&e->update_done[b], ef)) != cudaSuccess) return err;
+    if ((err = cudaEventCreateWithFlags(&e->buffer_free[b], ef)) != cudaSuccess) return err;
+  }
+  return cudaEventCreateWithFlags(&e->done, ef);
+}
+
+// Counts asynchronous enqueues so the test hook can fail the k-th one.
+struct Enqueuer {
+  int kind;
+  int64_t k;
+  int64_t count = 0;
+  bool injected = false;
+  cudaError_t operator()(cudaError_t (*issue)(void*), void* ctx) {
+    ++count;
+    if (kind == 1 && count == k) {
+      injected = true;
+      return cudaErrorUnknown;
+    }
+    return issue(ctx);
+  }
+};
+
+struct CopyOp {
+  void* dst;
+  const void* src;
+  size_t bytes;
+  cudaMemcpyKind dir;
+  cudaStream_t st;
+};
+static cudaError_t do_copy(void* p) {
+  CopyOp* c = static_cast<CopyOp*>(p);
+  return cudaMemcpyAsync(c->dst, c->src, c->bytes, c->dir, c->st);
+}
+struct RecordOp {
+  cudaEvent_t ev;
+  cudaStream_t st;
+};
+static cudaError_t do_record(void* p) {
+  RecordOp* r = static_cast<RecordOp*>(p);
+  return cudaEventRecord(r->ev, r->st);
+}
+static cudaError_t do_wait(void* p) {
+  RecordOp* r = static_cast<RecordOp*>(p);
+  return cudaStreamWaitEvent(r->st, r->ev, 0);
+}
+struct LaunchOp {
+  lst_format fmt;
+  Run run;
+  const Scalars* s;
+  cudaStream_t st;
+};
+static cudaError_t do_launch(void* p) {
+  LaunchOp* l = static_cast<LaunchOp*>(p);
+  return launch_update(l->fmt, false, &l->run, 1, *l->s, l->st);
+}
+
+static void drain(Engine* e) {
+  cudaStreamSynchronize(e->h2d);
+  cudaStreamSynchronize(e->compute);
+  cudaStreamSynchronize(e->d2h);
+}
+
+}  // namespace lst
+
+using namespace lst;
+
+extern "C" lst_status lst_stream_step(const lst_layout* Lc, void* const* host_blocks, void* dev_buf0,
+                                      void* dev_buf1, const lst_adamw_hparams* hp, int64_t timeout_ms) {
+  clear_error();
+  if (!Lc) return fail(LST_ERR_INVALID_ARG, "lst_stream_step: null layout");
+  if (!hp) return fail(LST_ERR_INVALID_ARG, "lst_stream_step: null hparams");
+  Scalars s;
+  if (!make_scalars(*hp, &s))
+    return fail(LST_ERR_INVALID_ARG,
+                "lst_stream_step: hyperparameters outside their domain (step >= 1, 0 <= beta < 1, finite)");
+  lst_layout* L = const_cast<lst_layout*>(Lc);  // engine cache and lock only
+  const int64_t n = (int64_t)L->blocks.size();
+  if (n == 0) return LST_OK;
+  if (!host_blocks) return fail(LST_ERR_INVALID_ARG, "lst_stream_step: host_blocks is null");
+  if (!dev_buf0 || !dev_buf1) return fail(LST_ERR_INVALID_ARG, "lst_stream_step: device buffer is null");
+  if (reinterpret_cast<uintptr_t>(dev_buf0) % 256 || reinterpret_cast<uintptr_t>(dev_buf1) % 256)
+    return fail(LST_ERR_ALIGNMENT, "lst_stream_step: device buffers must be 256-byte aligned");
+  for (int64_t i = 0; i < n; ++i) {
+    if (L->blocks[(size_t)i].bytes == 0) continue;
+    if (!host_blocks[i])
+      return fail(LST_ERR_INVALID_ARG, "lst_stream_step: host block %lld is null", (long long)i);
+    if (reinterpret_cast<uintptr_t>(host_blocks[i]) % 4096)
+      return fail(LST_ERR_ALIGNMENT, "lst_stream_step: host block %lld not 4096-byte aligned", (long long)i);
+  }
+  // Pinned / device checks (host-side driver queries, no device work).
+  for (int64_t i = 0; i < n; ++i) {
+    if (L->blocks[(size_t)i].bytes == 0) continue;
+    cudaPointerAttributes a;
+    cudaError_t err = cudaPointerGetAttributes(&a, host_blocks[i]);
+    if (err != cudaSuccess) {
+      cudaGetLastError();
+      return fail(LST_ERR_NOT_PINNED, "lst_stream_step: host block %lld is not pinned", (long long)i);
+    }
+    if (a.type != cudaMemoryTypeHost)
+      return fail(LST_ERR_NOT_PINNED, "lst_stream_step: host block %lld is not pinned host memory",
+                  (long long)i);
+  }
+  for (void* d : {dev_buf0, dev_buf1}) {
+    cudaPointerAttributes a;
+    cudaError_t err = cudaPointerGetAttributes(&a, d);
+    if (err != cudaSuccess) {
+      cudaGetLastError();
+      return fail(LST_ERR_INVALID_ARG, "lst_stream_step: device buffer is not device memory");
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+      return fail(LST_ERR_INVALID_ARG, "lst_stream_step: device buffer is not device memory");
+  }
+
+  std::lock_guard<std::mutex> guard(L->stream_mu);
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "lst_stream_step: cudaGetDevice");
+  if (L->engine && L->engine->device != dev) {
+    destroy_engine(L->engine);
+    L->engine = nullptr;
+  }
+  if (!L->engine) {
+    Engine* e = new (std::nothrow) Engine();
+    if (!e) return fail(LST_ERR_OOM, "lst_stream_step: out of host memory");
+    err = create(e, dev);
+    if (err != cudaSuccess) {
+      release(e);
+      delete e;
+      return cuda_fail(err, "lst_stream_step: creating streams/events");
+    }
+    L->engine = e;
+  }
+  Engine* E = L->engine;
+
+  const FormatInfo& fi = format_info(L->fmt);
+  Enqueuer enq{inject().kind.load(), inject().k.load()};
+  char* bufs[2] = {static_cast<char*>(dev_buf0), static_cast<char*>(dev_buf1)};
+  bool used[2] = {false, false};
+  const char* what = nullptr;
+
+  for (int64_t i = 0; i < n && !what; ++i) {
+    const Block& b = L->blocks[(size_t)i];
+    if (b.padded == 0) continue;
+    const int bi = (int)(i & 1);
+    char* buf = bufs[bi];
+    char* host = static_cast<char*>(host_blocks[i]);
+    if (used[bi]) {  // buffer-free: the last outbound copy from this buffer
+      RecordOp w{E->buffer_free[bi], E->h2d};
+      if ((err = enq(do_wait, &w)) != cudaSuccess) { what = "wait buffer-free"; break; }
+    }
+    used[bi] = true;
+    const int64_t C = (L->stream_chunk > 0 && L->stream_chunk < b.padded) ? L->stream_chunk : b.padded;
+    const bool whole = (C == b.padded);
+    for (int64_t e0 = 0; e0 < b.padded; e0 += C) {
+      const int64_t e1 = (e0 + C < b.padded) ? e0 + C : b.padded;
+      // StreamIn: the fields the update reads.
+      if (whole) {
+        CopyOp c{buf + b.h2d_off, host + b.h2d_off, (size_t)b.h2d_bytes, cudaMemcpyHostToDevice, E->h2d};
+        if ((err = enq(do_copy, &c)) != cudaSuccess) { what = "copy in"; break; }
+      } else {
+        for (int k = 0; k < fi.n_inputs && !what; ++k) {
+          const int64_t off = b.seg_off[fi.field[k]] + e0 * fi.elem_bytes[k];
+          CopyOp c{buf + off, host + off, (size_t)((e1 - e0) * fi.elem_bytes[k]), cudaMemcpyHostToDevice,
+                   E->h2d};
+          if ((err = enq(do_copy, &c)) != cudaSuccess) what = "copy in";
+        }
+        if (what) break;
+      }
+      RecordOp r1{E->weights_ready[bi], E->h2d};
+      if ((err = enq(do_record, &r1)) != cudaSuccess) { what = "record weights-ready"; break; }
+      RecordOp w1{E->weights_ready[bi], E->compute};
+      if ((err = enq(do_wait, &w1)) != cudaSuccess) { what = "wait weights-ready"; break; }
+      // The update on the staged chunk.
+      LaunchOp l{L->fmt, block_run(*L, b, buf, e0, e1), &s, E->compute};
+      if ((err = enq(do_launch, &l)) != cudaSuccess) { what = "launch update"; break; }
+      RecordOp r2{E->update_done[bi], E->compute};
+      if ((err = enq(do_record, &r2)) != cudaSuccess) { what = "record update-done"; break; }
+      RecordOp w2{E->update_done[bi], E->d2h};
+      if ((err = enq(do_wait, &w2)) != cudaSuccess) { what = "wait update-done"; break; }
+      // StreamOut: the fields the update wrote.
+      if (whole) {
+        CopyOp c{host + b.d2h_off, buf + b.d2h_off, (size_t)b.d2h_bytes, cudaMemcpyDeviceToHost, E->d2h};
+        if ((err = enq(do_copy, &c)) != cudaSuccess) { what = "copy out"; break; }
+      } else {
+        for (int k = fi.first_output; k < fi.n_segments && !what; ++k) {
+          const int64_t off = b.seg_off[fi.field[k]] + e0 * fi.elem_bytes[k];
+          CopyOp c{host + off, buf + off, (size_t)((e1 - e0) * fi.elem_bytes[k]), cudaMemcpyDeviceToHost,
+                   E->d2h};
+          if ((err = enq(do_copy, &c)) != cudaSuccess) what = "copy out";
+        }
+        if (what) break;
+      }
+    }
+    if (what) break;
+    RecordOp r3{E->buffer_free[bi], E->d2h};
+    if ((err = enq(do_record, &r3)) != cudaSuccess) { what = "record buffer-free"; break; }
+  }
+  if (!what) {
+    RecordOp rd{E->done, E->d2h};
+    if ((err = enq(do_record, &rd)) != cudaSuccess) what = "record done";
+  }
+  if (what) {
+    drain(E);  // nothing of this call stays in flight
+    if (enq.injected)
+      return fail(LST_ERR_CUDA, "lst_stream_step: %s: injected failure at enqueue %lld", what,
+                  (long long)enq.k);
+    return cuda_fail(err, what);
+  }
+
+  // Completion: poll the final event against the host-side deadline.
+  const bool never_done = (enq.kind == 2);
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    cudaError_t q = never_done ? cudaErrorNotReady : cudaEventQuery(E->done);
+    if (q == cudaSuccess) return LST_OK;
+    if (q != cudaErrorNotReady) {
+      drain(E);
+      return cuda_fail(q, "lst_stream_step: waiting for completion");
+    }
+    if (timeout_ms > 0 &&
+        std::chrono::steady_clock::now() - t0 >= std::chrono::milliseconds(timeout_ms)) {
+      if (never_done) drain(E);  // the simulated hang: the real work is finite
+      return fail(LST_ERR_TIMEOUT, "lst_stream_step: not complete after %lld ms", (long long)timeout_ms);
+    }
+    std::this_thread::sleep_for(std::chrono::microseconds(20));
+  }
+}

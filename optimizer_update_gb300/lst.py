@@ -1,0 +1,202 @@
+"""ctypes binding of liblst.so (include/lst.h), same names, argument marshalling only.
+
+Every computation happens in the library's CUDA kernels and copy engines.
+There is no fallback: if liblst.so has not been built, every call raises.
+Pointers are plain Python ints (e.g. ``tensor.data_ptr()``); streams are
+``cudaStream_t`` values as ints (e.g. ``torch.cuda.current_stream().cuda_stream``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence, Tuple
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblst.so")
+
+# lst_status
+LST_OK = 0
+LST_ERR_INVALID_ARG = 1
+LST_ERR_ALIGNMENT = 2
+LST_ERR_NOT_PINNED = 3
+LST_ERR_CUDA = 4
+LST_ERR_OOM = 5
+LST_ERR_TIMEOUT = 6
+# lst_format
+LST_L12_BF16 = 0
+LST_L16_MIXED = 1
+LST_L16_FP32 = 2
+# lst_field
+LST_FIELD_G = 0
+LST_FIELD_W = 1
+LST_FIELD_M = 2
+LST_FIELD_V = 3
+LST_FIELD_MASTER = 4
+
+FORMATS = {"L12": LST_L12_BF16, "L16M": LST_L16_MIXED, "L16F": LST_L16_FP32}
+FIELDS = {"G": LST_FIELD_G, "W": LST_FIELD_W, "M": LST_FIELD_M, "V": LST_FIELD_V, "MASTER": LST_FIELD_MASTER}
+
+
+class lst_adamw_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64)]
+
+
+def adamw_hparams(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1):
+    return lst_adamw_hparams(lr, beta1, beta2, eps, weight_decay, step)
+
+
+class LstError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} [status {status}]")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load liblst.so; raises if it is not built (no fallback path exists)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        i32, i64, vp, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
+        P = ctypes.POINTER
+        sig = {
+            "lst_layout_create": ([i32, P(i32), P(i64), P(i32), ctypes.c_int, P(vp)], ctypes.c_int),
+            "lst_layout_destroy": ([vp], None),
+            "lst_layout_info": ([vp, P(i64), P(i64), P(i64)], ctypes.c_int),
+            "lst_layout_block": ([vp, i64, P(i64), P(i64), P(i64)], ctypes.c_int),
+            "lst_layout_segment": ([vp, i64, i32, P(i64), P(i64)], ctypes.c_int),
+            "lst_layout_tensor": ([vp, i32, i32, P(i64), P(i64), P(i64)], ctypes.c_int),
+            "lst_layout_transfer": ([vp, i64, P(i64), P(i64), P(i64), P(i64)], ctypes.c_int),
+            "lst_layout_set_stream_chunk": ([vp, i64], ctypes.c_int),
+            "lst_adamw_step": ([vp, P(vp), P(lst_adamw_hparams), vp], ctypes.c_int),
+            "lst_sgd_step": ([vp, P(vp), f32, vp], ctypes.c_int),
+            "lst_stream_step": ([vp, P(vp), vp, vp, P(lst_adamw_hparams), i64], ctypes.c_int),
+            "lst_host_alloc": ([i64, P(vp)], ctypes.c_int),
+            "lst_host_free": ([vp], ctypes.c_int),
+            "lst_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "lst_last_error": ([], ctypes.c_char_p),
+            "lst_test_inject": ([i32, i64], ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != LST_OK:
+        msg = lib().lst_last_error().decode(errors="replace")
+        raise LstError(status, f"{lib().lst_status_string(status).decode()}: {msg}")
+
+
+def _ptr_array(ptrs: Sequence[int]):
+    arr = (ctypes.c_void_p * max(1, len(ptrs)))()
+    for i, p in enumerate(ptrs):
+        arr[i] = int(p) if p else None
+    return arr
+
+
+# ---------------------------------------------------------------------------
+def lst_layout_create(shapes: Sequence[Sequence[int]], layer_of_tensor: Sequence[int], fmt) -> int:
+    """shapes: one shape (0..4 dims) per tensor; returns the layout handle."""
+    fmt = FORMATS.get(fmt, fmt)
+    n = len(shapes)
+    if len(layer_of_tensor) != n:
+        raise ValueError("one block index per tensor")
+    ndim = (ctypes.c_int32 * max(1, n))()
+    dims = (ctypes.c_int64 * max(1, 4 * n))()
+    lay = (ctypes.c_int32 * max(1, n))()
+    for i, s in enumerate(shapes):
+        ndim[i] = len(s)
+        for k, d in enumerate(s[:4]):
+            dims[4 * i + k] = int(d)
+        if len(s) > 4:
+            ndim[i] = len(s)  # rejected by the library
+        lay[i] = int(layer_of_tensor[i])
+    out = ctypes.c_void_p()
+    _check(lib().lst_layout_create(n, ndim, dims, lay, int(fmt), ctypes.byref(out)))
+    return out.value
+
+
+def lst_layout_destroy(handle: int) -> None:
+    lib().lst_layout_destroy(handle)
+
+
+def lst_layout_info(handle: int) -> Tuple[int, int, int]:
+    a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().lst_layout_info(handle, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def lst_layout_block(handle: int, layer: int) -> Tuple[int, int, int]:
+    a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().lst_layout_block(handle, layer, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def lst_layout_segment(handle: int, layer: int, field) -> Tuple[int, int]:
+    field = FIELDS.get(field, field)
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().lst_layout_segment(handle, layer, int(field), ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def lst_layout_tensor(handle: int, tensor: int, field) -> Tuple[int, int, int]:
+    field = FIELDS.get(field, field)
+    a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().lst_layout_tensor(handle, tensor, int(field), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def lst_layout_transfer(handle: int, layer: int) -> Tuple[int, int, int, int]:
+    v = [ctypes.c_int64() for _ in range(4)]
+    _check(lib().lst_layout_transfer(handle, layer, *[ctypes.byref(x) for x in v]))
+    return tuple(x.value for x in v)
+
+
+def lst_layout_set_stream_chunk(handle: int, elems: int) -> None:
+    _check(lib().lst_layout_set_stream_chunk(handle, elems))
+
+
+def lst_adamw_step(handle: int, dev_blocks: Sequence[int], hparams: lst_adamw_hparams, stream: int = 0) -> None:
+    _check(lib().lst_adamw_step(handle, _ptr_array(dev_blocks), ctypes.byref(hparams), stream or None))
+
+
+def lst_sgd_step(handle: int, dev_blocks: Sequence[int], lr: float, stream: int = 0) -> None:
+    _check(lib().lst_sgd_step(handle, _ptr_array(dev_blocks), lr, stream or None))
+
+
+def lst_stream_step(handle: int, host_blocks: Sequence[int], dev_buf0: int, dev_buf1: int,
+                    hparams: lst_adamw_hparams, timeout_ms: int = 0) -> None:
+    _check(lib().lst_stream_step(handle, _ptr_array(host_blocks), dev_buf0, dev_buf1, ctypes.byref(hparams),
+                                 timeout_ms))
+
+
+def lst_host_alloc(nbytes: int) -> int:
+    out = ctypes.c_void_p()
+    _check(lib().lst_host_alloc(nbytes, ctypes.byref(out)))
+    return out.value
+
+
+def lst_host_free(ptr: int) -> None:
+    _check(lib().lst_host_free(ptr))
+
+
+def lst_status_string(status: int) -> str:
+    return lib().lst_status_string(status).decode()
+
+
+def lst_last_error() -> str:
+    return lib().lst_last_error().decode(errors="replace")
+
+
+def lst_test_inject(kind: int, k: int = 0) -> None:
+    _check(lib().lst_test_inject(kind, k))

@@ -134,6 +134,23 @@ def _kind(dist: str, dtype: str) -> int:
     return KIND_BF16 if dtype == "bf16" else KIND_F32
 
 
+def fill_field(arr: np.ndarray, field: str, fmt: str, spans: Sequence[Tuple[str, int, int]], layer: int,
+               workload: str, t: int, seed: int = DEFAULT_SEED, threads: int | None = None) -> None:
+    """Fill one field array of a block (padding set to zero)."""
+    dtype = dict(FORMAT_FIELDS[fmt])[field]
+    arr[...] = 0
+    if fmt == "L16M" and field == "W":
+        return  # the mixed layout's bf16 W is an output derived from MASTER
+    for (name, off, n) in spans:
+        if n == 0:
+            continue
+        dist, sigma = field_dist(workload, field, name, t)
+        if dist == "zero":
+            continue
+        fill(arr[off:off + n], _kind(dist, dtype), seed, stream_id(FIELD_CODES[field], layer), off, sigma,
+             threads)
+
+
 def fill_block(fields: Dict[str, np.ndarray], spans: Sequence[Tuple[str, int, int]], layer: int,
                workload: str, fmt: str, t: int, seed: int = DEFAULT_SEED,
                g_seed: int | None = None, threads: int | None = None) -> None:
@@ -145,20 +162,9 @@ def fill_block(fields: Dict[str, np.ndarray], spans: Sequence[Tuple[str, int, in
     Padding elements are set to zero. g_seed, if given, replaces the seed of the
     gradient field (a fresh gradient per step).
     """
-    for field, dtype in FORMAT_FIELDS[fmt]:
-        arr = fields[field]
-        arr[...] = 0
-        if fmt == "L16M" and field == "W":
-            continue  # the mixed layout's bf16 W is an output derived from MASTER
-        for (name, off, n) in spans:
-            if n == 0:
-                continue
-            dist, sigma = field_dist(workload, field, name, t)
-            if dist == "zero":
-                continue
-            s = g_seed if (field == "G" and g_seed is not None) else seed
-            fill(arr[off:off + n], _kind(dist, dtype), s, stream_id(FIELD_CODES[field], layer), off,
-                 sigma, threads)
+    for field, _ in FORMAT_FIELDS[fmt]:
+        s = g_seed if (field == "G" and g_seed is not None) else seed
+        fill_field(fields[field], field, fmt, spans, layer, workload, t, s, threads)
 
 
 def gather_block(field: str, fmt: str, spans: Sequence[Tuple[str, int, int]], layer: int,

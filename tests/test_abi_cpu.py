@@ -1,0 +1,164 @@
+"""The C ABI without a GPU: exported symbols, block geometry (bit-exact against
+the oracle's calculator), argument validation that happens before any CUDA
+call, status strings."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from oracle import layout as olayout
+from synth import shapes
+
+
+@pytest.fixture(scope="module")
+def L():
+    from optimizer_update_gb300 import lst
+    if not os.path.exists(lst.LIB_PATH):
+        from optimizer_update_gb300 import build
+        build.build()
+    return lst
+
+
+def _declared_symbols():
+    hdr = open(os.path.join(ROOT, "include", "lst.h")).read()
+    return sorted(set(re.findall(r"^LST_API [^;]*?\b(lst_\w+)\(", hdr, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = _declared_symbols()
+    assert len(names) >= 16
+    raw = ctypes.CDLL(L.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def _edge_specs():
+    return [
+        ("scalar", (), 0), ("one", (1,), 0), ("seven", (7,), 0), ("nine", (3, 3), 0),
+        ("tail", (4097,), 1), ("empty", (0, 5), 1), ("four_d", (2, 3, 4, 5), 1),
+    ]
+
+
+CASES = [(n, fn, fmt) for n, (fn, fmt) in shapes.WORKLOADS.items()] + [
+    ("edge_l12", _edge_specs, "L12"), ("edge_l16m", _edge_specs, "L16M"), ("edge_l16f", _edge_specs, "L16F"),
+    ("lora_as_l12", shapes.tinyllama_lora, "L12"), ("layer_as_l16m", shapes.tinyllama_layer, "L16M"),
+]
+
+
+@pytest.mark.parametrize("name,fn,fmt", CASES, ids=[c[0] for c in CASES])
+def test_layout_geometry_matches_oracle_bit_exact(L, name, fn, fmt):
+    specs = fn()
+    O = olayout.plan(specs, fmt)
+    h = L.lst_layout_create([s for (_, s, _) in specs], [l for (_, _, l) in specs], fmt)
+    try:
+        n_layers, n_params, max_bytes = L.lst_layout_info(h)
+        assert (n_layers, n_params, max_bytes) == (len(O.blocks), O.n_params, O.max_block_bytes)
+        for i, b in enumerate(O.blocks):
+            assert L.lst_layout_block(h, i) == (b.nbytes, b.params, b.padded)
+            for f, (off, size) in b.segments.items():
+                assert L.lst_layout_segment(h, i, f) == (off, size)
+            assert L.lst_layout_transfer(h, i) == (b.h2d[0], b.h2d[1], b.d2h[0], b.d2h[1])
+        for t in range(len(specs)):
+            for f in O.blocks[O.tensor_block[t]].segments:
+                off, layer, eoff = L.lst_layout_tensor(h, t, f)
+                assert off == O.tensor_byte_offset(t, f)
+                assert (layer, eoff) == (O.tensor_block[t], O.tensor_elem_offset[t])
+    finally:
+        L.lst_layout_destroy(h)
+
+
+def test_empty_layout(L):
+    h = L.lst_layout_create([], [], "L12")
+    assert L.lst_layout_info(h) == (0, 0, 0)
+    # a step over no blocks is a no-op and needs no device
+    L.lst_adamw_step(h, [], L.adamw_hparams(step=1))
+    L.lst_layout_destroy(h)
+
+
+@pytest.mark.parametrize("shapes_,layers,fmt", [
+    ([(1, 2, 3, 4, 5)], [0], "L12"),     # ndim 5
+    ([(-1,)], [0], "L12"),               # negative dim
+    ([(4,), (4,)], [0, 2], "L12"),       # block 1 has no tensors
+    ([(4,)], [-1], "L12"),               # negative block
+    ([(4,)], [0], 7),                    # unknown format
+    ([(1 << 21, 1 << 20)], [0], "L12"),  # 2^41 elements
+])
+def test_layout_create_rejects(L, shapes_, layers, fmt):
+    with pytest.raises(L.LstError) as e:
+        L.lst_layout_create(shapes_, layers, fmt)
+    assert e.value.status == L.LST_ERR_INVALID_ARG
+
+
+def test_geometry_queries_reject_out_of_range(L):
+    h = L.lst_layout_create([(8,)], [0], "L12")
+    try:
+        for call in (lambda: L.lst_layout_block(h, 1), lambda: L.lst_layout_segment(h, 0, "MASTER"),
+                     lambda: L.lst_layout_tensor(h, 1, "G"), lambda: L.lst_layout_transfer(h, -1),
+                     lambda: L.lst_layout_set_stream_chunk(h, 1000)):
+            with pytest.raises(L.LstError) as e:
+                call()
+            assert e.value.status == L.LST_ERR_INVALID_ARG
+        L.lst_layout_set_stream_chunk(h, 4096)
+        L.lst_layout_set_stream_chunk(h, 0)
+    finally:
+        L.lst_layout_destroy(h)
+
+
+def test_step_validation_before_any_cuda_call(L):
+    h = L.lst_layout_create([(8,)], [0], "L12")
+    try:
+        bad = [L.adamw_hparams(step=0), L.adamw_hparams(beta1=1.0), L.adamw_hparams(beta2=-0.1),
+               L.adamw_hparams(lr=float("nan")), L.adamw_hparams(eps=float("inf"))]
+        for hp in bad:
+            with pytest.raises(L.LstError) as e:
+                L.lst_adamw_step(h, [4096], hp)
+            assert e.value.status == L.LST_ERR_INVALID_ARG
+            with pytest.raises(L.LstError) as e:
+                L.lst_stream_step(h, [4096], 4096, 8192, hp)
+            assert e.value.status == L.LST_ERR_INVALID_ARG
+        with pytest.raises(L.LstError) as e:
+            L.lst_adamw_step(h, [4096 + 8], L.adamw_hparams())
+        assert e.value.status == L.LST_ERR_ALIGNMENT
+        with pytest.raises(L.LstError) as e:
+            L.lst_adamw_step(h, [0], L.adamw_hparams())
+        assert e.value.status == L.LST_ERR_INVALID_ARG
+        with pytest.raises(L.LstError) as e:
+            L.lst_sgd_step(h, [4096], float("inf"))
+        assert e.value.status == L.LST_ERR_INVALID_ARG
+        with pytest.raises(L.LstError) as e:
+            L.lst_stream_step(h, [4096 + 64], 4096, 8192, L.adamw_hparams())
+        assert e.value.status == L.LST_ERR_ALIGNMENT
+        with pytest.raises(L.LstError) as e:
+            L.lst_stream_step(h, [4096], 4096 + 16, 8192, L.adamw_hparams())
+        assert e.value.status == L.LST_ERR_ALIGNMENT
+        with pytest.raises(L.LstError) as e:
+            L.lst_stream_step(h, [4096], 0, 8192, L.adamw_hparams())
+        assert e.value.status == L.LST_ERR_INVALID_ARG
+    finally:
+        L.lst_layout_destroy(h)
+
+
+def test_status_strings_and_inject_validation(L):
+    for st in range(7):
+        assert L.lst_status_string(st)
+    assert L.lst_status_string(99) == "unknown status"
+    with pytest.raises(L.LstError):
+        L.lst_test_inject(5, 0)
+    with pytest.raises(L.LstError):
+        L.lst_test_inject(1, 0)
+    L.lst_test_inject(0, 0)
+    assert L.lst_last_error() == ""
+
+
+def test_product_does_not_reach_the_oracle():
+    """The product package never imports, loads or names the oracle."""
+    pkg = os.path.join(ROOT, "optimizer_update_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cpp", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f
+                assert "synth" not in text, f

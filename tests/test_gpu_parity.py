@@ -1,0 +1,196 @@
+"""Device-resident step vs the oracle, element by element (GB300).
+
+Small and medium workloads are compared in full; the full-size workloads
+(TinyLlama-1.1B mixed, LLaMA-7B) on sampled elements that the oracle computes
+one by one from the generator's inputs at those indices. Tolerances: fp32
+fields within 1e-6 relative (+1e-30 absolute), bf16 weights within one bf16
+ulp of the oracle's round-to-nearest-even result; the kernel is also expected
+to be bit-exact (same fp32 operation order, IEEE division and square root).
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from optimizer_update_gb300 import Layout, lst
+from synth import shapes
+
+from gpu_util import (FIELD_DT, compare, device_blocks, fill_host_block, gather_device, gathered_inputs,
+                      guards_intact, hparams_for, oracle_step, sample_indices)
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(autouse=True)
+def _need_cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _run_full(specs, fmt, workload, t, sgd=False, guard=4096, hp_override=None):
+    """Fill, step on the device, step the oracle, compare every field of every block."""
+    L = Layout(specs, fmt)
+    hosts = [np.empty(L.block_bytes(i), np.uint8) for i in range(L.n_layers)]
+    for i in range(L.n_layers):
+        fill_host_block(L, i, hosts[i], workload, t)
+    blocks, backing = device_blocks(L, guard=guard)
+    for i in range(L.n_layers):
+        blocks[i].copy_(torch.from_numpy(hosts[i]))
+    hp, ohp = hparams_for(workload, t)
+    if hp_override:
+        for k, v in hp_override.items():
+            setattr(hp, k, v)
+            setattr(ohp, k, v)
+    ptrs = [b.data_ptr() for b in blocks]
+    if sgd:
+        lst.lst_sgd_step(L.handle, ptrs, hp.lr, _stream())
+    else:
+        lst.lst_adamw_step(L.handle, ptrs, hp, _stream())
+    torch.cuda.synchronize()
+    stats = []
+    for i in range(L.n_layers):
+        before_g = L.numpy_views(i, hosts[i])["G"].copy()
+        oracle_step(L, hosts[i], i, ohp, sgd=sgd)
+        got = L.numpy_views(i, blocks[i].cpu().numpy())
+        exp = L.numpy_views(i, hosts[i])
+        fields = ("W",) if (sgd and fmt != "L16M") else (("MASTER", "W") if sgd else None)
+        s = compare(fmt, got, exp, fields)
+        assert np.array_equal(got["G"], before_g), "gradient must be read-only"
+        if sgd:  # moments untouched
+            assert np.array_equal(got["M"].view(np.uint32), exp["M"].view(np.uint32))
+            assert np.array_equal(got["V"].view(np.uint32), exp["V"].view(np.uint32))
+        stats.append(s)
+    if guard:
+        assert guards_intact(backing, L, guard), "write outside a block"
+    return L, stats
+
+
+def _assert_bit_exact(stats):
+    for s in stats:
+        for f, d in s.items():
+            assert d["bit_exact"] == d["n"], f"{f}: {d['n'] - d['bit_exact']} elements not bit-exact"
+
+
+# ---- one TinyLlama-1.1B decoder layer, 12 B/param, t = 1 (m = v = 0) and t = 10
+@pytest.mark.parametrize("t", [1, 10])
+def test_tinyllama_layer_l12_full(t):
+    _, stats = _run_full(shapes.tinyllama_layer(), "L12", "tinyllama_layer_l12", t)
+    _assert_bit_exact(stats)
+
+
+# ---- TinyLlama LoRA r=8 adapters (308 tensors, 22 blocks), fp32, multi-block launch
+@pytest.mark.parametrize("t", [1, 10])
+def test_tinyllama_lora_l16f_full(t):
+    # the frozen bf16 base (1.1B parameters) is resident but never passed to
+    # the library: it must come through bit-untouched
+    base = torch.randint(-32768, 32767, (1_100_048_384,), dtype=torch.int16, device="cuda")
+    ck = int(base.view(torch.int32)[: base.numel() // 2].sum(dtype=torch.int64))
+    _, stats = _run_full(shapes.tinyllama_lora(), "L16F", "tinyllama_lora_l16f", t)
+    _assert_bit_exact(stats)
+    assert int(base.view(torch.int32)[: base.numel() // 2].sum(dtype=torch.int64)) == ck
+    del base
+
+
+# ---- odd sizes: 1, 7, 9, 4097 elements, a scalar, an empty tensor, several blocks
+EDGE = [("scalar", (), 0), ("one", (1,), 0), ("seven", (7,), 0), ("nine", (9,), 1),
+        ("tail", (4097,), 1), ("empty", (0, 3), 2), ("x", (5, 3), 2), ("big", (70_001,), 3)]
+
+
+@pytest.mark.parametrize("fmt", ["L12", "L16M", "L16F"])
+@pytest.mark.parametrize("sgd", [False, True])
+def test_edge_shapes(fmt, sgd):
+    _, stats = _run_full(EDGE, fmt, "edge", 7, sgd=sgd)
+    _assert_bit_exact(stats)
+
+
+def test_mixed_layout_three_layers():
+    specs = [s for s in shapes.tinyllama_full() if s[2] in (1, 2, 3)]
+    specs = [(n, sh, l - 1) for (n, sh, l) in specs]
+    _, stats = _run_full(specs, "L16M", "tinyllama_full_l16m", 10)
+    _assert_bit_exact(stats)
+
+
+@pytest.mark.parametrize("fmt", ["L12", "L16M", "L16F"])
+def test_lr_zero_keeps_weights(fmt):
+    L = Layout(shapes.tinyllama_layer()[:3], fmt)
+    host = np.empty(L.block_bytes(0), np.uint8)
+    fill_host_block(L, 0, host, "lr0", 5)
+    blk = torch.from_numpy(host).cuda()
+    hp, _ = hparams_for("lr0", 5)
+    hp.lr = 0.0
+    lst.lst_adamw_step(L.handle, [blk.data_ptr()], hp, _stream())
+    torch.cuda.synchronize()
+    got, before = L.numpy_views(0, blk.cpu().numpy()), L.numpy_views(0, host)
+    wf = "MASTER" if fmt == "L16M" else "W"
+    # the input weights hold no -0.0 (lattice draws): w*1 - 0*u is w bit for bit
+    assert np.array_equal(got[wf].view(np.uint8), before[wf].view(np.uint8))
+    assert not np.array_equal(got["M"], before["M"]) and not np.array_equal(got["V"], before["V"])
+
+
+def test_more_blocks_than_one_launch_holds():
+    # 300 small blocks: the run table is split over several launches
+    specs = [(f"t{i}", (1000 + 37 * i,), i) for i in range(300)]
+    _, stats = _run_full(specs, "L12", "many", 3)
+    _assert_bit_exact(stats)
+
+
+def test_padding_stays_zero():
+    L = Layout([("a", (5,), 0), ("b", (3000,), 0)], "L16M")
+    host = np.zeros(L.block_bytes(0), np.uint8)
+    fill_host_block(L, 0, host, "pad", 4)
+    blk = torch.from_numpy(host).cuda()
+    lst.lst_adamw_step(L.handle, [blk.data_ptr()], hparams_for("pad", 4)[0], _stream())
+    torch.cuda.synchronize()
+    v = L.numpy_views(0, blk.cpu().numpy())
+    used = np.zeros(L.padded(0), bool)
+    for (_, off, n) in L.spans(0):
+        used[off:off + n] = True
+    for f, arr in v.items():
+        assert not np.any(arr[~used]), f
+
+
+# ---- full sizes, sampled (the launch configuration the bench times: one
+# multi-block launch over every block of the model)
+def _full_size_sampled(specs, fmt, workload, t, seed_rng):
+    L = Layout(specs, fmt)
+    host = np.empty(L.max_block_bytes, np.uint8)
+    blocks = []
+    for i in range(L.n_layers):
+        n = L.block_bytes(i)
+        fill_host_block(L, i, host[:n], workload, t)
+        b = torch.empty(n, dtype=torch.uint8, device="cuda")
+        b.copy_(torch.from_numpy(host[:n]))
+        blocks.append(b)
+    hp, ohp = hparams_for(workload, t)
+    lst.lst_adamw_step(L.handle, [b.data_ptr() for b in blocks], hp, _stream())
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(seed_rng)
+    checked = 0
+    for i in range(L.n_layers):
+        idx = sample_indices(L.padded(i), L.spans(i), rng)
+        inp = gathered_inputs(L, i, workload, t, idx)
+        oracle.step(fmt, inp, ohp)
+        got = gather_device(L.torch_views(i, blocks[i]), idx)
+        s = compare(fmt, got, inp)
+        _assert_bit_exact([s])
+        checked += idx.size
+    del blocks
+    return checked
+
+
+@pytest.mark.slow
+def test_tinyllama_full_l16m_sampled():
+    assert _full_size_sampled(shapes.tinyllama_full(), "L16M", "tinyllama_full_l16m", 10, 1) > 100_000
+
+
+@pytest.mark.slow
+def test_llama7b_l12_sampled():
+    assert _full_size_sampled(shapes.llama7b(), "L12", "llama7b_l12", 10, 2) > 100_000
