@@ -343,7 +343,7 @@ def run_ours(args):
     L = build_layout(args.workload, args.max_blocks)
     hp_kw = HP_LORA if L.fmt == "L16F" else HP
     P = L.n_params
-    chunk = 1 << 22
+    chunk = 1 << 24  # 16 Mi elements per sub-chunk (the library default)
     L.set_stream_chunk(chunk)
     ptrs, arrs = alloc_pinned_state(L, args.workload, seed)
 
@@ -461,7 +461,7 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="tinyllama_full_l16m")

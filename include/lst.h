@@ -159,7 +159,7 @@ LST_API lst_status lst_layout_transfer(const lst_layout* layout, int64_t layer, 
                                int64_t* h2d_bytes, int64_t* d2h_offset, int64_t* d2h_bytes);
 
 /* Element count of the sub-chunks the streamed step moves and updates at a
-   time (a multiple of 2048; 0 = one chunk per block). Default 4,194,304. */
+   time (a multiple of 2048; 0 = one chunk per block). Default 16,777,216. */
 LST_API lst_status lst_layout_set_stream_chunk(lst_layout* layout, int64_t elems);
 
 /* ------------------------------------------------------------------------
@@ -219,8 +219,11 @@ LST_API lst_status lst_stream_step(const lst_layout* layout, void* const* host_b
  * Utilities.
  * ------------------------------------------------------------------------ */
 
-/* Page-locked host memory (cudaHostAlloc), page aligned. Free with
-   lst_host_free. */
+/* Page-locked host memory: page-aligned (at least 4096 bytes) anonymous
+   memory registered with CUDA as mapped and portable, so a device kernel may
+   also address it directly. Free with lst_host_free (LST_ERR_INVALID_ARG for
+   a pointer that did not come from lst_host_alloc). LST_ERR_OOM if the memory
+   cannot be reserved or pinned. */
 LST_API lst_status lst_host_alloc(int64_t bytes, void** out);
 LST_API lst_status lst_host_free(void* ptr);
 

@@ -4,10 +4,24 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include <sys/mman.h>
+#include <unistd.h>
 
 #include "lst_internal.h"
 
 namespace lst {
+
+static std::unordered_map<void*, size_t>& host_allocs() {
+  static std::unordered_map<void*, size_t> m;
+  return m;
+}
+static std::mutex& host_allocs_mu() {
+  static std::mutex m;
+  return m;
+}
 
 static thread_local char g_err[512] = "";
 
@@ -112,28 +126,50 @@ extern "C" lst_status lst_sgd_step(const lst_layout* L, void* const* dev_blocks,
   return device_step(L, dev_blocks, s, true, cuda_stream, "lst_sgd_step");
 }
 
+// Pinned host memory for blocks: page-aligned anonymous memory registered with
+// CUDA (mapped and portable), so every block starts on a page boundary
+// whatever its size (small cudaHostAlloc allocations need not be page aligned).
 extern "C" lst_status lst_host_alloc(int64_t bytes, void** out) {
   clear_error();
   if (!out) return fail(LST_ERR_INVALID_ARG, "lst_host_alloc: out is null");
   *out = nullptr;
   if (bytes <= 0) return fail(LST_ERR_INVALID_ARG, "lst_host_alloc: bytes must be > 0");
-  cudaError_t err = cudaHostAlloc(out, (size_t)bytes, cudaHostAllocDefault);
-  if (err == cudaErrorMemoryAllocation) {
-    cudaGetLastError();
-    *out = nullptr;
-    return fail(LST_ERR_OOM, "lst_host_alloc: %lld bytes: out of pinned host memory", (long long)bytes);
-  }
+  long page = sysconf(_SC_PAGESIZE);
+  if (page < 4096) page = 4096;
+  const size_t size = ((size_t)bytes + (size_t)page - 1) / (size_t)page * (size_t)page;
+  void* p = mmap(nullptr, size, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+  if (p == MAP_FAILED) return fail(LST_ERR_OOM, "lst_host_alloc: %lld bytes: out of host memory", (long long)bytes);
+  cudaError_t err = cudaHostRegister(p, size, cudaHostRegisterMapped | cudaHostRegisterPortable);
   if (err != cudaSuccess) {
-    *out = nullptr;
+    munmap(p, size);
+    if (err == cudaErrorMemoryAllocation) {
+      cudaGetLastError();
+      return fail(LST_ERR_OOM, "lst_host_alloc: %lld bytes: cannot pin", (long long)bytes);
+    }
     return cuda_fail(err, "lst_host_alloc");
   }
+  {
+    std::lock_guard<std::mutex> g(host_allocs_mu());
+    host_allocs()[p] = size;
+  }
+  *out = p;
   return LST_OK;
 }
 
 extern "C" lst_status lst_host_free(void* p) {
   clear_error();
   if (!p) return LST_OK;
-  cudaError_t err = cudaFreeHost(p);
+  size_t size = 0;
+  {
+    std::lock_guard<std::mutex> g(host_allocs_mu());
+    auto it = host_allocs().find(p);
+    if (it == host_allocs().end())
+      return fail(LST_ERR_INVALID_ARG, "lst_host_free: pointer not from lst_host_alloc");
+    size = it->second;
+    host_allocs().erase(it);
+  }
+  cudaError_t err = cudaHostUnregister(p);
+  munmap(p, size);
   if (err != cudaSuccess) return cuda_fail(err, "lst_host_free");
   return LST_OK;
 }

@@ -18,7 +18,7 @@ constexpr int64_t kTensorAlign = 8;     // elements: 16 B in a bf16 segment
 constexpr int64_t kBlockAlign = 2048;   // elements: every segment a whole number of 4 KB pages
 constexpr int64_t kWarpSpan = 256;      // elements one warp covers per task (kernel tiling)
 constexpr int64_t kMaxBlockElems = int64_t(1) << 40;
-constexpr int64_t kDefaultStreamChunk = int64_t(1) << 22;
+constexpr int64_t kDefaultStreamChunk = int64_t(1) << 24;
 
 // Segment order and element size of each format.
 struct FormatInfo {

@@ -11,7 +11,7 @@
 //
 // GB300 specifics. The host link (NVLink-C2C on Grace systems) is duplex, so
 // the inbound and outbound copies of different sub-chunks overlap. Each block
-// is moved in sub-chunks (the layout's stream chunk, default 4 Mi elements):
+// is moved in sub-chunks (the layout's stream chunk, default 16 Mi elements):
 // chunk c's update starts as soon as chunk c has arrived and its outbound copy
 // as soon as its update is done, so the pipeline fills and drains in one
 // sub-chunk rather than one whole block. Block i is staged in buffer i & 1 at
