@@ -165,14 +165,21 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def kernel_source_sha() -> str:
+    """Hash of the sources of the device-resident update kernel."""
+    h = hashlib.sha256()
+    for f in ("lst_device.cuh", "lst_kernels.cu"):
+        h.update(open(os.path.join(ROOT, "optimizer_update_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def kernel_traffic(params: int):
     """DRAM bytes per launch of the update kernel from the committed ncu
     summary, scaled to `params`; None if the kernel source changed since."""
-    src = os.path.join(ROOT, "optimizer_update_gb300", "csrc", "lst_kernels.cu")
     summ = os.path.join(ROOT, "profiles", "lst_update_kernel_traffic.txt")
     if not os.path.exists(summ):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = kernel_source_sha()
     vals = {}
     for line in open(summ):
         p = line.split()

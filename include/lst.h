@@ -185,6 +185,47 @@ LST_API lst_status lst_sgd_step(const lst_layout* layout, void* const* dev_block
                         void* cuda_stream);
 
 /* ------------------------------------------------------------------------
+ * Per-block options: step counters, locked blocks, gradient magnitude.
+ * ("Training 70B Models on Consumer Hardware", section "Progressive Layer
+ * Locking": a layer whose gradient magnitude falls below a threshold is
+ * locked - no update and no I/O for it; and the note under "The Math": with
+ * locking, per-layer step counters keep Adam's bias correction exact.)
+ * ------------------------------------------------------------------------ */
+typedef struct lst_step_options {
+  /* Host array [n_layers] of per-block step counters t_i >= 1 for the bias
+     corrections, or NULL: hparams->step for every block. */
+  const int64_t* block_steps;
+  /* Host array [n_layers]; a nonzero entry marks a locked block: it is neither
+     read nor written (and, in the streamed step, not transferred). NULL: none. */
+  const uint8_t* skip;
+  /* DEVICE array [n_layers] of doubles, or NULL. When given, every block that
+     is not skipped receives sum(g^2) over its elements (its squared gradient
+     L2 norm), computed in the same pass as the update: per group of 8
+     elements in fp32, accumulated in fp64 in a fixed order (deterministic for
+     a given device). Entries of skipped blocks are left untouched. Written
+     asynchronously on the call's stream. */
+  double* grad_sq;
+  /* DEVICE scratch of lst_workspace_bytes() bytes, 256-byte aligned; required
+     when grad_sq is given. Calls that share a workspace must not overlap on
+     the GPU. The library sets what must start at zero before each launch. */
+  void* workspace;
+} lst_step_options;
+
+/* Bytes of device workspace the sum-of-squares reduction needs (a constant:
+   one fp64 partial per CTA, up to 1024 CTAs, and per block of one launch, up
+   to 128 blocks, plus a 256-byte header). */
+LST_API int64_t lst_workspace_bytes(void);
+
+/* lst_adamw_step with per-block options (opts may be NULL). Results of a
+   block with step t_i are bit-identical to lst_adamw_step on that block alone
+   with step = t_i. Errors as lst_adamw_step, plus LST_ERR_INVALID_ARG for a
+   block step < 1 or grad_sq without workspace, LST_ERR_ALIGNMENT for a
+   misaligned workspace or grad_sq. */
+LST_API lst_status lst_adamw_step_ex(const lst_layout* layout, void* const* dev_blocks,
+                                     const lst_adamw_hparams* hparams, const lst_step_options* opts,
+                                     void* cuda_stream);
+
+/* ------------------------------------------------------------------------
  * Streamed step ("MegaTrain" summary page: host memory is the authoritative
  * store; StreamIn over a weight stream, compute, offload over a second copy
  * stream; two buffers ping-pong; events weights-ready, update-done and
@@ -214,6 +255,30 @@ LST_API lst_status lst_sgd_step(const lst_layout* layout, void* const* dev_block
    as failed as a whole), LST_ERR_TIMEOUT. */
 LST_API lst_status lst_stream_step(const lst_layout* layout, void* const* host_blocks, void* dev_buf0,
                            void* dev_buf1, const lst_adamw_hparams* hparams, int64_t timeout_ms);
+
+/* lst_stream_step with per-block options (opts may be NULL). A locked block
+   (skip) is not transferred in either direction and not updated. grad_sq is
+   a device array; it is complete when the call returns LST_OK. Results of
+   every block are bit-identical to lst_adamw_step_ex on the same data. */
+LST_API lst_status lst_stream_step_ex(const lst_layout* layout, void* const* host_blocks, void* dev_buf0,
+                                      void* dev_buf1, const lst_adamw_hparams* hparams,
+                                      const lst_step_options* opts, int64_t timeout_ms);
+
+/* One AdamW step with the update kernel reading and writing the pinned host
+   blocks in place over the host link (NVLink-C2C on Grace systems): no device
+   buffers, no copy engines. This is the zero-copy staging the "MegaTrain"
+   summary page mentions for its 4 KB-aligned blocks, taken to its end: the
+   kernel is the only consumer of the staged bytes, so it may as well read
+   them where they are. Results are bit-identical to lst_adamw_step.
+   host_blocks: n_layers pointers to page-locked host memory that is mapped
+   into the device address space (lst_host_alloc, cudaHostAlloc, or
+   cudaHostRegister with cudaHostRegisterMapped), each 4096-byte aligned.
+   Asynchronous on cuda_stream, like lst_adamw_step; the host must not touch
+   the blocks until the stream has passed the step.
+   Errors: LST_ERR_INVALID_ARG, LST_ERR_ALIGNMENT, LST_ERR_NOT_PINNED (not
+   pinned, or not mapped), LST_ERR_CUDA. */
+LST_API lst_status lst_zero_copy_step(const lst_layout* layout, void* const* host_blocks,
+                                      const lst_adamw_hparams* hparams, void* cuda_stream);
 
 /* ------------------------------------------------------------------------
  * Utilities.

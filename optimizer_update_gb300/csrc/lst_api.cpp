@@ -129,6 +129,117 @@ extern "C" lst_status lst_sgd_step(const lst_layout* L, void* const* dev_blocks,
 // Pinned host memory for blocks: page-aligned anonymous memory registered with
 // CUDA (mapped and portable), so every block starts on a page boundary
 // whatever its size (small cudaHostAlloc allocations need not be page aligned).
+extern "C" int64_t lst_workspace_bytes(void) { return kWorkspaceBytes; }
+
+namespace lst {
+
+// Validates the options against the layout and builds, for every block that
+// is not skipped, its bias corrections. Returns LST_OK or an error status.
+lst_status prepare_options(const lst_layout* L, const lst_adamw_hparams& hp, const lst_step_options* o,
+                           std::vector<float>* bc1, std::vector<float>* bc2, const char* who) {
+  const int64_t n = (int64_t)L->blocks.size();
+  bc1->assign((size_t)n, 0.0f);
+  bc2->assign((size_t)n, 0.0f);
+  if (o && o->grad_sq) {
+    if (!o->workspace) return fail(LST_ERR_INVALID_ARG, "%s: grad_sq needs a workspace", who);
+    if (reinterpret_cast<uintptr_t>(o->workspace) % 256)
+      return fail(LST_ERR_ALIGNMENT, "%s: workspace not 256-byte aligned", who);
+    if (reinterpret_cast<uintptr_t>(o->grad_sq) % 8)
+      return fail(LST_ERR_ALIGNMENT, "%s: grad_sq not 8-byte aligned", who);
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    if (o && o->skip && o->skip[i]) continue;
+    lst_adamw_hparams h = hp;
+    if (o && o->block_steps) h.step = o->block_steps[i];
+    Scalars s;
+    if (!make_scalars(h, &s))
+      return fail(LST_ERR_INVALID_ARG, "%s: block %lld: step must be >= 1", who, (long long)i);
+    (*bc1)[(size_t)i] = s.bias_correction1;
+    (*bc2)[(size_t)i] = s.bias_correction2;
+  }
+  return LST_OK;
+}
+
+}  // namespace lst
+
+extern "C" lst_status lst_adamw_step_ex(const lst_layout* L, void* const* dev_blocks, const lst_adamw_hparams* hp,
+                                        const lst_step_options* opts, void* cuda_stream) {
+  clear_error();
+  if (!L) return fail(LST_ERR_INVALID_ARG, "lst_adamw_step_ex: null layout");
+  if (!hp) return fail(LST_ERR_INVALID_ARG, "lst_adamw_step_ex: null hparams");
+  Scalars s;
+  if (!make_scalars(*hp, &s))
+    return fail(LST_ERR_INVALID_ARG,
+                "lst_adamw_step_ex: hyperparameters outside their domain (step >= 1, 0 <= beta < 1, finite)");
+  std::vector<float> bc1, bc2;
+  lst_status st = prepare_options(L, *hp, opts, &bc1, &bc2, "lst_adamw_step_ex");
+  if (st != LST_OK) return st;
+  const int64_t n = (int64_t)L->blocks.size();
+  if (n == 0) return LST_OK;
+  if (!dev_blocks) return fail(LST_ERR_INVALID_ARG, "lst_adamw_step_ex: dev_blocks is null");
+  const bool want_sq = opts && opts->grad_sq;
+  std::vector<RunEx> runs;
+  for (int64_t i = 0; i < n; ++i) {
+    if (opts && opts->skip && opts->skip[i]) continue;
+    const Block& b = L->blocks[(size_t)i];
+    if (b.bytes > 0) {
+      if (!dev_blocks[i])
+        return fail(LST_ERR_INVALID_ARG, "lst_adamw_step_ex: block %lld pointer is null", (long long)i);
+      if (reinterpret_cast<uintptr_t>(dev_blocks[i]) % 16 != 0)
+        return fail(LST_ERR_ALIGNMENT, "lst_adamw_step_ex: block %lld pointer not 16-byte aligned", (long long)i);
+    }
+    RunEx r;
+    r.run = block_run(*L, b, static_cast<char*>(dev_blocks[i]), 0, b.padded);
+    r.bias_correction1 = bc1[(size_t)i];
+    r.bias_correction2 = bc2[(size_t)i];
+    r.out_index = want_sq ? (int32_t)i : -1;
+    r.accumulate = 0;
+    if (r.run.elems == 0 && !want_sq) continue;
+    runs.push_back(r);
+  }
+  if (runs.empty()) return LST_OK;
+  cudaError_t err = launch_update_ex(L->fmt, runs.data(), (int)runs.size(), s, want_sq ? opts->workspace : nullptr,
+                                     want_sq ? opts->grad_sq : nullptr, static_cast<cudaStream_t>(cuda_stream));
+  if (err != cudaSuccess) return cuda_fail(err, "lst_adamw_step_ex");
+  return LST_OK;
+}
+
+// Zero-copy step: the update kernel addresses the pinned, mapped host blocks
+// directly, so every byte crosses the host link exactly once in each needed
+// direction and neither device buffers nor copy engines are involved.
+extern "C" lst_status lst_zero_copy_step(const lst_layout* L, void* const* host_blocks,
+                                         const lst_adamw_hparams* hp, void* cuda_stream) {
+  clear_error();
+  if (!L) return fail(LST_ERR_INVALID_ARG, "lst_zero_copy_step: null layout");
+  if (!hp) return fail(LST_ERR_INVALID_ARG, "lst_zero_copy_step: null hparams");
+  Scalars s;
+  if (!make_scalars(*hp, &s))
+    return fail(LST_ERR_INVALID_ARG,
+                "lst_zero_copy_step: hyperparameters outside their domain (step >= 1, 0 <= beta < 1, finite)");
+  const int64_t n = (int64_t)L->blocks.size();
+  if (n == 0) return LST_OK;
+  if (!host_blocks) return fail(LST_ERR_INVALID_ARG, "lst_zero_copy_step: host_blocks is null");
+  std::vector<void*> dptr((size_t)n, nullptr);
+  for (int64_t i = 0; i < n; ++i) {
+    if (L->blocks[(size_t)i].bytes == 0) continue;
+    if (!host_blocks[i])
+      return fail(LST_ERR_INVALID_ARG, "lst_zero_copy_step: host block %lld is null", (long long)i);
+    if (reinterpret_cast<uintptr_t>(host_blocks[i]) % 4096)
+      return fail(LST_ERR_ALIGNMENT, "lst_zero_copy_step: host block %lld not 4096-byte aligned", (long long)i);
+    cudaPointerAttributes a;
+    cudaError_t err = cudaPointerGetAttributes(&a, host_blocks[i]);
+    if (err != cudaSuccess) {
+      cudaGetLastError();
+      return fail(LST_ERR_NOT_PINNED, "lst_zero_copy_step: host block %lld is not pinned", (long long)i);
+    }
+    if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr)
+      return fail(LST_ERR_NOT_PINNED, "lst_zero_copy_step: host block %lld is not pinned, mapped host memory",
+                  (long long)i);
+    dptr[(size_t)i] = a.devicePointer;
+  }
+  return device_step(L, dptr.data(), s, false, cuda_stream, "lst_zero_copy_step");
+}
+
 extern "C" lst_status lst_host_alloc(int64_t bytes, void** out) {
   clear_error();
   if (!out) return fail(LST_ERR_INVALID_ARG, "lst_host_alloc: out is null");

@@ -19,6 +19,7 @@ constexpr int64_t kBlockAlign = 2048;   // elements: every segment a whole numbe
 constexpr int64_t kWarpSpan = 256;      // elements one warp covers per task (kernel tiling)
 constexpr int64_t kMaxBlockElems = int64_t(1) << 40;
 constexpr int64_t kDefaultStreamChunk = int64_t(1) << 24;
+constexpr int kMaxRunsPerLaunch = 128;
 
 // Segment order and element size of each format.
 struct FormatInfo {
@@ -93,7 +94,24 @@ Run block_run(const lst_layout& L, const Block& b, char* base, int64_t e0, int64
 // runs). Returns the first CUDA error, cudaSuccess otherwise.
 cudaError_t launch_update(lst_format fmt, bool sgd, const Run* runs, int n_runs, const Scalars& s,
                           cudaStream_t stream);
-constexpr int kMaxRunsPerLaunch = 128;
+
+// A run of the extended update: per-run bias corrections and, optionally,
+// the slot of grad_sq that receives the run's sum of g^2.
+struct RunEx {
+  Run run;
+  float bias_correction1, bias_correction2;
+  int32_t out_index;   // -1: no sum
+  int32_t accumulate;  // 1: add to the slot, 0: overwrite it
+};
+
+// Workspace of the sum-of-squares reduction: a counter, then one fp64
+// partial per (run, CTA) of a launch.
+constexpr int kMaxGridEx = 1024;
+constexpr int64_t kWorkspaceHeader = 256;
+constexpr int64_t kWorkspaceBytes = kWorkspaceHeader + int64_t(8) * kMaxGridEx * kMaxRunsPerLaunch;
+
+cudaError_t launch_update_ex(lst_format fmt, const RunEx* runs, int n_runs, const Scalars& s, void* workspace,
+                             double* grad_sq, cudaStream_t stream);
 
 // Error reporting (thread-local text).
 lst_status fail(lst_status st, const char* fmt, ...);
@@ -108,5 +126,8 @@ struct Inject {
 Inject& inject();
 
 void destroy_engine(Engine* e);
+
+lst_status prepare_options(const lst_layout* L, const lst_adamw_hparams& hp, const lst_step_options* o,
+                           std::vector<float>* bc1, std::vector<float>* bc2, const char* who);
 
 }  // namespace lst

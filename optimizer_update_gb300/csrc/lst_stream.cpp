@@ -120,9 +120,14 @@ struct LaunchOp {
   Run run;
   const Scalars* s;
   cudaStream_t st;
+  bool ex;          // per-block options in use: the extended kernel
+  RunEx run_ex;
+  void* workspace;
+  double* grad_sq;
 };
 static cudaError_t do_launch(void* p) {
   LaunchOp* l = static_cast<LaunchOp*>(p);
+  if (l->ex) return launch_update_ex(l->fmt, &l->run_ex, 1, *l->s, l->workspace, l->grad_sq, l->st);
   return launch_update(l->fmt, false, &l->run, 1, *l->s, l->st);
 }
 
@@ -136,9 +141,8 @@ static void drain(Engine* e) {
 
 using namespace lst;
 
-extern "C" lst_status lst_stream_step(const lst_layout* Lc, void* const* host_blocks, void* dev_buf0,
-                                      void* dev_buf1, const lst_adamw_hparams* hp, int64_t timeout_ms) {
-  clear_error();
+static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, void* dev_buf0, void* dev_buf1,
+                              const lst_adamw_hparams* hp, const lst_step_options* opts, int64_t timeout_ms) {
   if (!Lc) return fail(LST_ERR_INVALID_ARG, "lst_stream_step: null layout");
   if (!hp) return fail(LST_ERR_INVALID_ARG, "lst_stream_step: null hparams");
   Scalars s;
@@ -146,6 +150,14 @@ extern "C" lst_status lst_stream_step(const lst_layout* Lc, void* const* host_bl
     return fail(LST_ERR_INVALID_ARG,
                 "lst_stream_step: hyperparameters outside their domain (step >= 1, 0 <= beta < 1, finite)");
   lst_layout* L = const_cast<lst_layout*>(Lc);  // engine cache and lock only
+  std::vector<float> bc1, bc2;
+  if (opts) {
+    lst_status st = prepare_options(L, *hp, opts, &bc1, &bc2, "lst_stream_step");
+    if (st != LST_OK) return st;
+  }
+  const bool ex = opts != nullptr;
+  const bool want_sq = opts && opts->grad_sq;
+  auto skipped = [&](int64_t i) { return opts && opts->skip && opts->skip[i]; };
   const int64_t n = (int64_t)L->blocks.size();
   if (n == 0) return LST_OK;
   if (!host_blocks) return fail(LST_ERR_INVALID_ARG, "lst_stream_step: host_blocks is null");
@@ -153,7 +165,7 @@ extern "C" lst_status lst_stream_step(const lst_layout* Lc, void* const* host_bl
   if (reinterpret_cast<uintptr_t>(dev_buf0) % 256 || reinterpret_cast<uintptr_t>(dev_buf1) % 256)
     return fail(LST_ERR_ALIGNMENT, "lst_stream_step: device buffers must be 256-byte aligned");
   for (int64_t i = 0; i < n; ++i) {
-    if (L->blocks[(size_t)i].bytes == 0) continue;
+    if (L->blocks[(size_t)i].bytes == 0 || skipped(i)) continue;
     if (!host_blocks[i])
       return fail(LST_ERR_INVALID_ARG, "lst_stream_step: host block %lld is null", (long long)i);
     if (reinterpret_cast<uintptr_t>(host_blocks[i]) % 4096)
@@ -161,7 +173,7 @@ extern "C" lst_status lst_stream_step(const lst_layout* Lc, void* const* host_bl
   }
   // Pinned / device checks (host-side driver queries, no device work).
   for (int64_t i = 0; i < n; ++i) {
-    if (L->blocks[(size_t)i].bytes == 0) continue;
+    if (L->blocks[(size_t)i].bytes == 0 || skipped(i)) continue;
     cudaPointerAttributes a;
     cudaError_t err = cudaPointerGetAttributes(&a, host_blocks[i]);
     if (err != cudaSuccess) {
@@ -212,7 +224,16 @@ extern "C" lst_status lst_stream_step(const lst_layout* Lc, void* const* host_bl
 
   for (int64_t i = 0; i < n && !what; ++i) {
     const Block& b = L->blocks[(size_t)i];
-    if (b.padded == 0) continue;
+    if (skipped(i)) continue;  // a locked block: no transfer, no update
+    if (b.padded == 0) {
+      if (want_sq) {  // an empty block's sum of squares is 0
+        LaunchOp l{L->fmt, block_run(*L, b, bufs[(int)(i & 1)], 0, 0), &s, E->compute, true, {}, opts->workspace,
+                   opts->grad_sq};
+        l.run_ex = RunEx{l.run, bc1[(size_t)i], bc2[(size_t)i], (int32_t)i, 0};
+        if ((err = enq(do_launch, &l)) != cudaSuccess) { what = "launch update"; break; }
+      }
+      continue;
+    }
     const int bi = (int)(i & 1);
     char* buf = bufs[bi];
     char* host = static_cast<char*>(host_blocks[i]);
@@ -243,7 +264,12 @@ extern "C" lst_status lst_stream_step(const lst_layout* Lc, void* const* host_bl
       RecordOp w1{E->weights_ready[bi], E->compute};
       if ((err = enq(do_wait, &w1)) != cudaSuccess) { what = "wait weights-ready"; break; }
       // The update on the staged chunk.
-      LaunchOp l{L->fmt, block_run(*L, b, buf, e0, e1), &s, E->compute};
+      LaunchOp l{L->fmt, block_run(*L, b, buf, e0, e1), &s, E->compute, ex, {}, nullptr, nullptr};
+      if (ex) {
+        l.run_ex = RunEx{l.run, bc1[(size_t)i], bc2[(size_t)i], want_sq ? (int32_t)i : -1, e0 > 0 ? 1 : 0};
+        l.workspace = want_sq ? opts->workspace : nullptr;
+        l.grad_sq = want_sq ? opts->grad_sq : nullptr;
+      }
       if ((err = enq(do_launch, &l)) != cudaSuccess) { what = "launch update"; break; }
       RecordOp r2{E->update_done[bi], E->compute};
       if ((err = enq(do_record, &r2)) != cudaSuccess) { what = "record update-done"; break; }
@@ -296,4 +322,17 @@ extern "C" lst_status lst_stream_step(const lst_layout* Lc, void* const* host_bl
     }
     std::this_thread::sleep_for(std::chrono::microseconds(20));
   }
+}
+
+extern "C" lst_status lst_stream_step(const lst_layout* L, void* const* host_blocks, void* dev_buf0, void* dev_buf1,
+                                      const lst_adamw_hparams* hp, int64_t timeout_ms) {
+  clear_error();
+  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, nullptr, timeout_ms);
+}
+
+extern "C" lst_status lst_stream_step_ex(const lst_layout* L, void* const* host_blocks, void* dev_buf0,
+                                         void* dev_buf1, const lst_adamw_hparams* hp, const lst_step_options* opts,
+                                         int64_t timeout_ms) {
+  clear_error();
+  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, opts, timeout_ms);
 }

@@ -43,6 +43,31 @@ class lst_adamw_hparams(ctypes.Structure):
                 ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64)]
 
 
+class lst_step_options(ctypes.Structure):
+    _fields_ = [("block_steps", ctypes.c_void_p), ("skip", ctypes.c_void_p), ("grad_sq", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p)]
+
+
+def step_options(block_steps=None, skip=None, grad_sq: int = 0, workspace: int = 0):
+    """Per-block options. block_steps / skip: sequences (host) of n_layers ints,
+    or None; grad_sq / workspace: device pointers (ints) or 0. The returned
+    structure keeps the host arrays alive."""
+    o = lst_step_options()
+    keep = []
+    if block_steps is not None:
+        a = (ctypes.c_int64 * max(1, len(block_steps)))(*[int(x) for x in block_steps])
+        keep.append(a)
+        o.block_steps = ctypes.cast(a, ctypes.c_void_p)
+    if skip is not None:
+        a = (ctypes.c_uint8 * max(1, len(skip)))(*[1 if x else 0 for x in skip])
+        keep.append(a)
+        o.skip = ctypes.cast(a, ctypes.c_void_p)
+    o.grad_sq = grad_sq or None
+    o.workspace = workspace or None
+    o._keep = keep
+    return o
+
+
 def adamw_hparams(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1):
     return lst_adamw_hparams(lr, beta1, beta2, eps, weight_decay, step)
 
@@ -77,6 +102,11 @@ def lib() -> ctypes.CDLL:
             "lst_adamw_step": ([vp, P(vp), P(lst_adamw_hparams), vp], ctypes.c_int),
             "lst_sgd_step": ([vp, P(vp), f32, vp], ctypes.c_int),
             "lst_stream_step": ([vp, P(vp), vp, vp, P(lst_adamw_hparams), i64], ctypes.c_int),
+            "lst_zero_copy_step": ([vp, P(vp), P(lst_adamw_hparams), vp], ctypes.c_int),
+            "lst_adamw_step_ex": ([vp, P(vp), P(lst_adamw_hparams), P(lst_step_options), vp], ctypes.c_int),
+            "lst_stream_step_ex": ([vp, P(vp), vp, vp, P(lst_adamw_hparams), P(lst_step_options), i64],
+                                   ctypes.c_int),
+            "lst_workspace_bytes": ([], i64),
             "lst_host_alloc": ([i64, P(vp)], ctypes.c_int),
             "lst_host_free": ([vp], ctypes.c_int),
             "lst_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -178,6 +208,27 @@ def lst_stream_step(handle: int, host_blocks: Sequence[int], dev_buf0: int, dev_
                     hparams: lst_adamw_hparams, timeout_ms: int = 0) -> None:
     _check(lib().lst_stream_step(handle, _ptr_array(host_blocks), dev_buf0, dev_buf1, ctypes.byref(hparams),
                                  timeout_ms))
+
+
+def lst_zero_copy_step(handle: int, host_blocks: Sequence[int], hparams: lst_adamw_hparams,
+                       stream: int = 0) -> None:
+    _check(lib().lst_zero_copy_step(handle, _ptr_array(host_blocks), ctypes.byref(hparams), stream or None))
+
+
+def lst_workspace_bytes() -> int:
+    return int(lib().lst_workspace_bytes())
+
+
+def lst_adamw_step_ex(handle: int, dev_blocks: Sequence[int], hparams: lst_adamw_hparams, opts=None,
+                      stream: int = 0) -> None:
+    _check(lib().lst_adamw_step_ex(handle, _ptr_array(dev_blocks), ctypes.byref(hparams),
+                                   ctypes.byref(opts) if opts is not None else None, stream or None))
+
+
+def lst_stream_step_ex(handle: int, host_blocks: Sequence[int], dev_buf0: int, dev_buf1: int,
+                       hparams: lst_adamw_hparams, opts=None, timeout_ms: int = 0) -> None:
+    _check(lib().lst_stream_step_ex(handle, _ptr_array(host_blocks), dev_buf0, dev_buf1, ctypes.byref(hparams),
+                                    ctypes.byref(opts) if opts is not None else None, timeout_ms))
 
 
 def lst_host_alloc(nbytes: int) -> int:

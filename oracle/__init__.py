@@ -55,6 +55,10 @@ def lib():
         L.orc_sgd_l16f.argtypes = [i64, vp, vp, f32]
         L.orc_bf16_from_f32_array.argtypes = [i64, vp, vp]
         L.orc_f32_from_bf16_array.argtypes = [i64, vp, vp]
+        L.orc_grad_sq_bf16.argtypes = [i64, vp]
+        L.orc_grad_sq_bf16.restype = ctypes.c_double
+        L.orc_grad_sq_f32.argtypes = [i64, vp]
+        L.orc_grad_sq_f32.restype = ctypes.c_double
         for fn in ("orc_adamw_l12", "orc_adamw_l16m", "orc_adamw_l16f", "orc_sgd_l12", "orc_sgd_l16m",
                    "orc_sgd_l16f", "orc_bf16_from_f32_array", "orc_f32_from_bf16_array"):
             getattr(L, fn).restype = None
@@ -178,3 +182,13 @@ def step(fmt: str, fields: dict, hp: Hparams, sgd: bool = False, threads: Option
             adamw_l16f(fields["G"], fields["W"], fields["M"], fields["V"], hp, threads)
     else:
         raise ValueError(fmt)
+
+
+def grad_sq(G: np.ndarray) -> float:
+    """Sum of g^2 over a gradient array (bf16 bits as uint16, or fp32), in fp64."""
+    G = np.ascontiguousarray(G)
+    if G.dtype == np.uint16:
+        return float(lib().orc_grad_sq_bf16(G.size, G.ctypes.data))
+    if G.dtype == np.float32:
+        return float(lib().orc_grad_sq_f32(G.size, G.ctypes.data))
+    raise TypeError(G.dtype)

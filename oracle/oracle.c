@@ -180,3 +180,27 @@ void orc_sgd_l16m(int64_t n, const uint16_t* G, float* master, uint16_t* W, floa
 void orc_sgd_l16f(int64_t n, const float* G, float* W, float lr) {
   for (int64_t i = 0; i < n; ++i) W[i] = sgd_one(G[i], W[i], lr);
 }
+
+/* ---- gradient magnitude for progressive layer locking -------------------- */
+
+/* Sum of g^2 over a block's gradient, in double, element by element in order
+   ("Training 70B Models on Consumer Hardware", section "Progressive Layer
+   Locking": a layer is locked when its gradient magnitude falls below a
+   threshold; the squared L2 norm is the plain reading of that magnitude). */
+double orc_grad_sq_bf16(int64_t n, const uint16_t* G) {
+  double s = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    double g = (double)orc_bf16_to_f32(G[i]);
+    s += g * g;
+  }
+  return s;
+}
+
+double orc_grad_sq_f32(int64_t n, const float* G) {
+  double s = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    double g = (double)G[i];
+    s += g * g;
+  }
+  return s;
+}

@@ -162,3 +162,25 @@ def test_product_does_not_reach_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f
                 assert "synth" not in text, f
+
+
+def test_step_options_validation_before_any_cuda_call(L):
+    h = L.lst_layout_create([(8,), (8,)], [0, 1], "L12")
+    try:
+        assert L.lst_workspace_bytes() == 256 + 8 * 1024 * 128
+        with pytest.raises(L.LstError) as e:  # a block step of 0
+            L.lst_adamw_step_ex(h, [4096, 8192], L.adamw_hparams(), L.step_options(block_steps=[1, 0]))
+        assert e.value.status == L.LST_ERR_INVALID_ARG
+        with pytest.raises(L.LstError) as e:  # grad_sq without a workspace
+            L.lst_adamw_step_ex(h, [4096, 8192], L.adamw_hparams(), L.step_options(grad_sq=4096))
+        assert e.value.status == L.LST_ERR_INVALID_ARG
+        with pytest.raises(L.LstError) as e:  # misaligned workspace
+            L.lst_adamw_step_ex(h, [4096, 8192], L.adamw_hparams(), L.step_options(grad_sq=4096, workspace=4096 + 64))
+        assert e.value.status == L.LST_ERR_ALIGNMENT
+        # a skipped block's bad step counter is never looked at; all blocks skipped: nothing to do
+        L.lst_adamw_step_ex(h, [0, 0], L.adamw_hparams(), L.step_options(block_steps=[0, 0], skip=[1, 1]))
+        with pytest.raises(L.LstError) as e:
+            L.lst_stream_step_ex(h, [4096, 8192], 4096, 8192, L.adamw_hparams(), L.step_options(block_steps=[0, 1]))
+        assert e.value.status == L.LST_ERR_INVALID_ARG
+    finally:
+        L.lst_layout_destroy(h)

@@ -207,3 +207,49 @@ def test_never_observed_completion_times_out():
         lst.lst_stream_step(L.handle, P.ptrs, b0.data_ptr(), b1.data_ptr(), lst.adamw_hparams(), 60_000)
     finally:
         P.free()
+
+
+# ---- zero-copy: the kernel works on the pinned host blocks over the link ----
+def _zero_copy_vs_device(specs, fmt, workload, t, steps):
+    L = Layout(specs, fmt)
+    P = PinnedBlocks(L)
+    try:
+        for i in range(L.n_layers):
+            fill_host_block(L, i, P.arrays[i], workload, t)
+        dev = [torch.from_numpy(P.arrays[i].copy()).cuda() for i in range(L.n_layers)]
+        ref = [P.arrays[i].copy() for i in range(L.n_layers)]
+        s = torch.cuda.current_stream().cuda_stream
+        for k in range(steps):
+            hp, ohp = hparams_for(workload, t + k)
+            lst.lst_adamw_step(L.handle, [d.data_ptr() for d in dev], hp, s)
+            lst.lst_zero_copy_step(L.handle, P.ptrs, hp, s)
+            torch.cuda.synchronize()
+            for i in range(L.n_layers):
+                oracle_step(L, ref[i], i, ohp)
+        for i in range(L.n_layers):
+            assert np.array_equal(P.arrays[i], dev[i].cpu().numpy()), f"block {i}: zero-copy differs"
+            compare(fmt, L.numpy_views(i, P.arrays[i]), L.numpy_views(i, ref[i]))
+    finally:
+        P.free()
+
+
+@pytest.mark.parametrize("fmt,workload", FMTS)
+def test_zero_copy_bit_identical(fmt, workload):
+    _zero_copy_vs_device(_three_tinyllama_layers(), fmt, workload, 10, steps=2)
+
+
+def test_zero_copy_lora_many_blocks():
+    _zero_copy_vs_device(shapes.tinyllama_lora(), "L16F", "tinyllama_lora_l16f", 1, steps=2)
+
+
+def test_zero_copy_rejects_pageable_and_device_memory():
+    L = _small()
+    pageable = [np.zeros(L.block_bytes(i) + 8192, np.uint8) for i in range(L.n_layers)]
+    ptrs = [(a.ctypes.data + 4095) // 4096 * 4096 for a in pageable]
+    with pytest.raises(lst.LstError) as e:
+        lst.lst_zero_copy_step(L.handle, ptrs, lst.adamw_hparams(), 0)
+    assert e.value.status == lst.LST_ERR_NOT_PINNED
+    d = [torch.empty(L.block_bytes(i), dtype=torch.uint8, device="cuda") for i in range(L.n_layers)]
+    with pytest.raises(lst.LstError) as e:
+        lst.lst_zero_copy_step(L.handle, [x.data_ptr() for x in d], lst.adamw_hparams(), 0)
+    assert e.value.status == lst.LST_ERR_NOT_PINNED

@@ -369,3 +369,22 @@ def test_general_step_within_rounding_bound_of_exact(t):
         wx = w1 - st
         e_w = U * abs(float(w1)) + float(lr) * e_u + U * abs(float(st)) + U * abs(float(wx))
         assert abs(float(W[i]) - float(wx)) <= 1.01 * e_w + 1e-45, (i, float(W[i]), float(wx), e_w)
+
+
+# ---------------------------------------------------------------------------
+# Gradient magnitude (progressive layer locking): sum of g^2 per block.
+# ---------------------------------------------------------------------------
+def test_grad_sq_closed_form_and_library():
+    # g = k / 64 for k = 1..n: sum of squares = n(n+1)(2n+1)/6 / 4096, exact in fp64
+    n = 2000
+    g = (np.arange(1, n + 1) / 64.0).astype(F32)
+    assert oracle.grad_sq(g) == n * (n + 1) * (2 * n + 1) / 6 / 4096
+    gb = oracle.bf16_from_f32((np.arange(1, 201) / 8.0).astype(F32))  # exact in bf16
+    assert oracle.grad_sq(gb) == 200 * 201 * 401 / 6 / 64
+    rng = np.random.default_rng(41)
+    x = (rng.standard_normal(100_000) * 1e-3).astype(F32)
+    assert oracle.grad_sq(x) == pytest.approx(float(np.sum(x.astype(np.float64) ** 2)), rel=1e-12)
+    xb = oracle.bf16_from_f32(x)
+    assert oracle.grad_sq(xb) == pytest.approx(float(np.sum(oracle.f32_from_bf16(xb).astype(np.float64) ** 2)),
+                                               rel=1e-12)
+    assert oracle.grad_sq(np.zeros(0, F32)) == 0.0
