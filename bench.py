@@ -16,6 +16,9 @@ zero moments.
   roofline  the fused update kernel against the measured HBM copy bandwidth.
   stream    pinned host-link bandwidth measured in the same run (H2D, D2H,
             both at once) and the streamed step against it.
+  zero_copy the same step with the update kernel reading and writing the
+            pinned host blocks directly (lst_zero_copy_step), against the
+            same link roofline.
   cpu_baseline  the oracle (plain C, all host cores) on a bounded sample.
 
 `--impl reference` times the oracle alone on the host, on the same workload.
@@ -407,7 +410,10 @@ def run_ours(args):
     # ---- streamed leg (the public end-to-end call) ------------------------------
     h2d_b = sum(L.transfer(i)[1] for i in range(L.n_layers))
     d2h_b = sum(L.transfer(i)[3] for i in range(L.n_layers))
-    for _ in range(max(1, min(args.warmup, 2))):
+    # the first steps over freshly pinned blocks run slower (address
+    # translations for the host pages are being set up): at least three
+    # untimed steps
+    for _ in range(max(3, min(args.warmup, 5))):
         lst.lst_stream_step(L.handle, ptrs, buf0.data_ptr(), buf1.data_ptr(),
                             lst.adamw_hparams(step=t, **hp_kw), 600_000)
         t += 1
@@ -428,6 +434,25 @@ def run_ours(args):
                        achieved_d2h_gbs=d2h_b * e_steps / t_e2e / 1e9,
                        roofline_ms=1e3 * roof_t, frac_of_link_roofline=roof_t / (t_e2e / e_steps),
                        chunk_elems=chunk)
+
+    # ---- zero-copy leg: the update kernel directly on the pinned host blocks ----
+    zstream = torch.cuda.Stream(device=device)
+    for _ in range(3):
+        lst.lst_zero_copy_step(L.handle, ptrs, lst.adamw_hparams(step=t, **hp_kw), zstream.cuda_stream)
+        t += 1
+    torch.cuda.synchronize(device)
+    barrier(device)
+    zs, ze = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    zs.record(zstream)
+    for _ in range(e_steps):
+        lst.lst_zero_copy_step(L.handle, ptrs, lst.adamw_hparams(step=t, **hp_kw), zstream.cuda_stream)
+        t += 1
+    ze.record(zstream)
+    torch.cuda.synchronize(device)
+    t_zc = max_over_ranks(zs.elapsed_time(ze) / 1e3, device)
+    zero_copy = {"value": world * P * e_steps / t_zc, "unit": "params/s", "call": "lst_zero_copy_step",
+                 "step_ms": 1e3 * t_zc / e_steps, "link_bytes_per_step": h2d_b + d2h_b,
+                 "frac_of_link_roofline": roof_t / (t_zc / e_steps), "steps": e_steps}
 
     # ---- CPU baseline: the oracle on the host cores, bounded sample ------------
     cpu = None
@@ -454,6 +479,7 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h_b, "steps": e_steps, "call": "lst_stream_step",
                     "gpu_launches": e_steps * chunks},
             "stream": stream_info,
+            "zero_copy": zero_copy,
             "cpu_baseline": cpu,
             "clocks": clk,
             "gpu_launches": args.steps,
