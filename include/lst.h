@@ -226,6 +226,40 @@ LST_API lst_status lst_adamw_step_ex(const lst_layout* layout, void* const* dev_
                                      void* cuda_stream);
 
 /* ------------------------------------------------------------------------
+ * For callers that cannot allocate device memory. The pages have no
+ * counterpart to this call; it exists so that the library can be used where
+ * device allocation is not available to the caller.
+ * ------------------------------------------------------------------------ */
+
+/* lst_adamw_step_ex, with the scratch of its sum-of-squares reduction taken
+   from memory the library holds itself instead of a caller's workspace.
+   It is meant for callers that cannot allocate device memory when they step
+   the optimizer: a plugin running inside an application whose device memory
+   belongs to another allocator, a training loop that has handed all device
+   memory to a framework's caching pool, or code that must not allocate once
+   it is running.
+   The scratch is one static device array of lst_workspace_bytes() bytes
+   (1 MiB + 256 bytes). Every GPU that loads the library's device code holds
+   it until the process exits. It holds the partial sums of one launch, so
+   when grad_sq is given at most 128 blocks may be updated per call (blocks
+   marked in skip do not count); more gives LST_ERR_INVALID_ARG and touches
+   nothing. Without grad_sq no scratch is used and there is no limit.
+   The first call on a device that passes grad_sq looks up the array's device
+   address (cudaGetSymbolAddress) with that device current; make that first
+   call before any stream capture. The call allocates nothing: no cudaMalloc,
+   no cudaFree, no allocating library routine.
+   All calls share the one array, which keeps the last call's contents; the
+   library zeroes what must start at zero before each launch. Calls whose
+   work overlaps on the GPU (streams with no ordering between them) race on
+   the array: order them, or use lst_adamw_step_ex with separate workspaces.
+   block_steps, skip: host arrays of n_layers entries, or NULL; grad_sq: a
+   device array of n_layers doubles, or NULL. Results are those of
+   lst_adamw_step_ex with the same arguments. Errors as lst_adamw_step_ex. */
+LST_API lst_status lst_adamw_step_ex_noalloc(const lst_layout* layout, void* const* dev_blocks,
+                                             const lst_adamw_hparams* hparams, const int64_t* block_steps,
+                                             const uint8_t* skip, double* grad_sq, void* cuda_stream);
+
+/* ------------------------------------------------------------------------
  * Streamed step ("MegaTrain" summary page: host memory is the authoritative
  * store; StreamIn over a weight stream, compute, offload over a second copy
  * stream; two buffers ping-pong; events weights-ready, update-done and

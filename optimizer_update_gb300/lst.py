@@ -107,6 +107,7 @@ def lib() -> ctypes.CDLL:
             "lst_stream_step_ex": ([vp, P(vp), vp, vp, P(lst_adamw_hparams), P(lst_step_options), i64],
                                    ctypes.c_int),
             "lst_workspace_bytes": ([], i64),
+            "lst_adamw_step_ex_noalloc": ([vp, P(vp), P(lst_adamw_hparams), vp, vp, vp, vp], ctypes.c_int),
             "lst_host_alloc": ([i64, P(vp)], ctypes.c_int),
             "lst_host_free": ([vp], ctypes.c_int),
             "lst_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -223,6 +224,17 @@ def lst_adamw_step_ex(handle: int, dev_blocks: Sequence[int], hparams: lst_adamw
                       stream: int = 0) -> None:
     _check(lib().lst_adamw_step_ex(handle, _ptr_array(dev_blocks), ctypes.byref(hparams),
                                    ctypes.byref(opts) if opts is not None else None, stream or None))
+
+
+def lst_adamw_step_ex_noalloc(handle: int, dev_blocks: Sequence[int], hparams: lst_adamw_hparams,
+                              block_steps=None, skip=None, grad_sq: int = 0, stream: int = 0) -> None:
+    """The extended step using the library's own static scratch (no allocation)."""
+    bs = (ctypes.c_int64 * max(1, len(block_steps)))(*[int(x) for x in block_steps]) if block_steps is not None else None
+    sk = (ctypes.c_uint8 * max(1, len(skip)))(*[1 if x else 0 for x in skip]) if skip is not None else None
+    _check(lib().lst_adamw_step_ex_noalloc(handle, _ptr_array(dev_blocks), ctypes.byref(hparams),
+                                           ctypes.cast(bs, ctypes.c_void_p) if bs is not None else None,
+                                           ctypes.cast(sk, ctypes.c_void_p) if sk is not None else None,
+                                           grad_sq or None, stream or None))
 
 
 def lst_stream_step_ex(handle: int, host_blocks: Sequence[int], dev_buf0: int, dev_buf1: int,
