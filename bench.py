@@ -19,6 +19,8 @@ zero moments.
   zero_copy the same step with the update kernel reading and writing the
             pinned host blocks directly (lst_zero_copy_step), against the
             same link roofline.
+  stream_devgrad  the streamed step with the gradients already on the device
+            (lst_stream_step_devgrad): 12 B/param inbound instead of 14.
   cpu_baseline  the oracle (plain C, all host cores) on a bounded sample.
 
 `--impl reference` times the oracle alone on the host, on the same workload.
@@ -51,6 +53,7 @@ WORKLOADS = {
     "tinyllama_layer_l12": ("tinyllama_layer", "L12", "one TinyLlama-1.1B decoder layer, 12 B/param"),
     "tinyllama_lora_l16f": ("tinyllama_lora", "L16F", "TinyLlama-1.1B LoRA r=8 adapters, fp32, 22 blocks"),
     "llama7b_l12": ("llama7b", "L12", "LLaMA-7B shape, 12 B/param, 34 blocks"),
+    "llama70b_slice8_l12": ("llama70b_slice", "L12", "Llama-70B depth slice, 8 decoder layers, 12 B/param"),
 }
 # Algorithmic bytes per parameter of one device-resident step (reads + writes).
 ALG_BYTES = {"L12": 22, "L16M": 28, "L16F": 28}
@@ -435,6 +438,35 @@ def run_ours(args):
                        roofline_ms=1e3 * roof_t, frac_of_link_roofline=roof_t / (t_e2e / e_steps),
                        chunk_elems=chunk)
 
+    # ---- streamed leg with device-resident gradients: only the state crosses
+    # the link inbound (the gradients stand for what a backward pass leaves on
+    # the device; producing them is not part of the timed step) ---------------
+    grads = []
+    for i in range(L.n_layers):
+        goff, gbytes = L.segment(i, "G")
+        g = torch.empty(gbytes, dtype=torch.uint8, device=device)
+        g.copy_(torch.from_numpy(arrs[i][goff:goff + gbytes]))
+        grads.append(g)
+    gptrs = [g.data_ptr() for g in grads]
+    dg_h2d = sum(L.transfer(i)[1] - L.segment(i, "G")[1] for i in range(L.n_layers))
+    for _ in range(3):
+        lst.lst_stream_step_devgrad(L.handle, ptrs, gptrs, buf0.data_ptr(), buf1.data_ptr(),
+                                    lst.adamw_hparams(step=t, **hp_kw), None, 600_000)
+        t += 1
+    barrier(device)
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        lst.lst_stream_step_devgrad(L.handle, ptrs, gptrs, buf0.data_ptr(), buf1.data_ptr(),
+                                    lst.adamw_hparams(step=t, **hp_kw), None, 600_000)
+        t += 1
+    t_dg = max_over_ranks(time.perf_counter() - t0, device)
+    roof_dg = max(dg_h2d / (link["h2d_concurrent_gbs"] * 1e9), d2h_b / (link["d2h_concurrent_gbs"] * 1e9))
+    stream_devgrad = {"value": world * P * e_steps / t_dg, "unit": "params/s", "call": "lst_stream_step_devgrad",
+                      "step_ms": 1e3 * t_dg / e_steps, "h2d_bytes_per_step": dg_h2d, "d2h_bytes_per_step": d2h_b,
+                      "roofline_ms": 1e3 * roof_dg, "frac_of_link_roofline": roof_dg / (t_dg / e_steps),
+                      "steps": e_steps}
+    del grads
+
     # ---- zero-copy leg: the update kernel directly on the pinned host blocks ----
     zstream = torch.cuda.Stream(device=device)
     for _ in range(3):
@@ -480,6 +512,7 @@ def run_ours(args):
                     "gpu_launches": e_steps * chunks},
             "stream": stream_info,
             "zero_copy": zero_copy,
+            "stream_devgrad": stream_devgrad,
             "cpu_baseline": cpu,
             "clocks": clk,
             "gpu_launches": args.steps,

@@ -83,7 +83,8 @@ typedef enum lst_status {
   LST_ERR_NOT_PINNED = 3,  /* host block not page-locked (pinned) host memory */
   LST_ERR_CUDA = 4,        /* a CUDA runtime call failed; see lst_last_error() */
   LST_ERR_OOM = 5,         /* host allocation failed */
-  LST_ERR_TIMEOUT = 6      /* lst_stream_step's host-side deadline passed */
+  LST_ERR_TIMEOUT = 6,     /* lst_stream_step's host-side deadline passed */
+  LST_ERR_IO = 7           /* a block file could not be read, written or flushed */
 } lst_status;
 
 typedef enum lst_format {
@@ -101,6 +102,7 @@ typedef enum lst_field {
 } lst_field;
 
 typedef struct lst_layout lst_layout; /* opaque, owned by the library */
+typedef struct lst_store lst_store;   /* opaque, owned by the library */
 
 /* AdamW hyperparameters. step = t >= 1, the global step counter ("The Math":
    one scalar t for all layers, incremented each batch). 0 <= beta < 1;
@@ -298,6 +300,27 @@ LST_API lst_status lst_stream_step_ex(const lst_layout* layout, void* const* hos
                                       void* dev_buf1, const lst_adamw_hparams* hparams,
                                       const lst_step_options* opts, int64_t timeout_ms);
 
+/* The streamed step for gradients that are already on the device, as a
+   backward pass leaves them. The "MegaTrain" page offloads gradients to the
+   host after backward (three-stream execution: a gradient stream for the
+   device-to-host offload) because its optimizer runs on the CPU; with the
+   update on the GPU the gradient never has to leave the device, so only the
+   state crosses the link inbound (L12: W|m|v, 10 B/param; L16M:
+   master|m|v, 12 B/param; L16F: W|m|v, 12 B/param), and the outbound bytes
+   are unchanged.
+   dev_grads: n_layers device pointers (16-byte aligned; ignored for skipped
+   or empty blocks), each to a block's gradient laid out as its G segment:
+   padded_elems elements of the G type (bf16, or fp32 for LST_L16_FP32), with
+   zeros in the padding. The G segments of the host blocks are neither read
+   nor written. The gradients must be complete when the call is made: the
+   call does not wait on other streams. opts may be NULL. Otherwise as
+   lst_stream_step_ex; results are bit-identical to it when the host G
+   segments hold the same gradient. */
+LST_API lst_status lst_stream_step_devgrad(const lst_layout* layout, void* const* host_blocks,
+                                           const void* const* dev_grads, void* dev_buf0, void* dev_buf1,
+                                           const lst_adamw_hparams* hparams, const lst_step_options* opts,
+                                           int64_t timeout_ms);
+
 /* One AdamW step with the update kernel reading and writing the pinned host
    blocks in place over the host link (NVLink-C2C on Grace systems): no device
    buffers, no copy engines. This is the zero-copy staging the "MegaTrain"
@@ -313,6 +336,68 @@ LST_API lst_status lst_stream_step_ex(const lst_layout* layout, void* const* hos
    pinned, or not mapped), LST_ERR_CUDA. */
 LST_API lst_status lst_zero_copy_step(const lst_layout* layout, void* const* host_blocks,
                                       const lst_adamw_hparams* hparams, void* cuda_stream);
+
+/* ------------------------------------------------------------------------
+ * File-backed block store: the tier under host memory. ("Training 70B Models
+ * on Consumer Hardware": model state in per-layer files on an SSD,
+ * pre-allocated with fallocate, flushed after each update, and - its safety
+ * note - a persisted step counter and atomic writes or shadow copies so that a
+ * crash cannot corrupt state. The "MegaTrain" summary page: SSDs as the next
+ * tier below host memory.)
+ * A store is a directory with one file per block: a 4096-byte header (magic,
+ * the layout's fingerprint for that block, the block's step counter, a header
+ * checksum) followed by the block's bytes. Files are read and written with
+ * direct I/O when the file system allows it. A block is committed by writing
+ * a shadow file, flushing it (fsync), renaming it over the block file and
+ * flushing the directory, so after a crash every block is at its old or its
+ * new step, never torn. The layout must outlive the store.
+ * ------------------------------------------------------------------------ */
+
+/* Create (or overwrite) a store in directory dir (created if missing, one
+   level) with every block at step counter `step` (>= 0). host_blocks: NULL
+   (blocks start zeroed) or n_layers host pointers, each 4096-byte aligned (a
+   NULL entry gives a zeroed block). Errors: LST_ERR_INVALID_ARG,
+   LST_ERR_ALIGNMENT, LST_ERR_IO, LST_ERR_OOM. */
+LST_API lst_status lst_store_create(const lst_layout* layout, const char* dir, void* const* host_blocks,
+                                    int64_t step, lst_store** out);
+
+/* Open an existing store. Every block file's header must match the layout
+   (LST_ERR_INVALID_ARG otherwise; LST_ERR_IO for a missing or damaged file).
+   A shadow file left by an interrupted commit is discarded: the block file
+   still holds the committed state. */
+LST_API lst_status lst_store_open(const lst_layout* layout, const char* dir, lst_store** out);
+
+/* Release the handle (the files stay). NULL is ignored. */
+LST_API void lst_store_close(lst_store* store);
+
+/* The step counter a block was last committed with. */
+LST_API lst_status lst_store_block_step(const lst_store* store, int64_t layer, int64_t* step);
+
+/* Read a block's bytes into host memory (4096-byte aligned, at least the
+   block's size), e.g. to inspect it or to write a gradient into its G
+   segment. */
+LST_API lst_status lst_store_read(const lst_store* store, int64_t layer, void* host_dst);
+
+/* Commit a block's bytes from host memory (4096-byte aligned) with step
+   counter `step` (>= 0), atomically as described above. */
+LST_API lst_status lst_store_write(lst_store* store, int64_t layer, const void* host_src, int64_t step);
+
+/* One AdamW step (hparams->step = t >= 1) over every block of the store whose
+   committed step counter is t - 1: read it from its file, update it with the
+   streamed step (lst_stream_step_ex on that block, through dev_buf0/dev_buf1),
+   commit it with step counter t. Blocks already at step t or beyond are
+   skipped, so a step that failed or was interrupted is completed by calling it
+   again with the same arguments: each block is updated exactly once. A block
+   below t - 1 has missed a step: LST_ERR_INVALID_ARG before anything is done.
+   The gradient is whatever the block file's G segment holds.
+   staging: three pinned host buffers (lst_host_alloc), each 4096-byte aligned
+   and at least max_block_bytes long; reading block k+1, updating block k and
+   committing block k-1 overlap on them. dev_buf0/1 and timeout_ms as in
+   lst_stream_step (the deadline applies per block). Synchronous. Errors: those
+   of lst_stream_step, plus LST_ERR_IO; after an error, blocks committed so far
+   are at step t and the others at t - 1. */
+LST_API lst_status lst_store_step(lst_store* store, void* const* staging, void* dev_buf0, void* dev_buf1,
+                                  const lst_adamw_hparams* hparams, int64_t timeout_ms);
 
 /* ------------------------------------------------------------------------
  * Utilities.
@@ -337,7 +422,10 @@ LST_API const char* lst_last_error(void);
    record or wait; counted from 1 within each later lst_stream_step call)
    reports a failure instead of being issued. kind 2: lst_stream_step never
    observes completion, so it returns LST_ERR_TIMEOUT at its deadline (after
-   which it still drains its own work before returning). */
+   which it still drains its own work before returning). kind 3: committing
+   block k-1 of a store (lst_store_write, lst_store_step) fails after its
+   shadow file is written and flushed, before the rename, as a crash there
+   would. */
 LST_API lst_status lst_test_inject(int32_t kind, int64_t k);
 
 #ifdef __cplusplus

@@ -294,6 +294,7 @@ extern "C" const char* lst_status_string(lst_status st) {
     case LST_ERR_CUDA: return "CUDA error";
     case LST_ERR_OOM: return "out of memory";
     case LST_ERR_TIMEOUT: return "timed out";
+    case LST_ERR_IO: return "file I/O error";
   }
   return "unknown status";
 }
@@ -302,8 +303,8 @@ extern "C" const char* lst_last_error(void) { return g_err; }
 
 extern "C" lst_status lst_test_inject(int32_t kind, int64_t k) {
   clear_error();
-  if (kind < 0 || kind > 2) return fail(LST_ERR_INVALID_ARG, "lst_test_inject: unknown kind %d", kind);
-  if (kind == 1 && k < 1) return fail(LST_ERR_INVALID_ARG, "lst_test_inject: k must be >= 1");
+  if (kind < 0 || kind > 3) return fail(LST_ERR_INVALID_ARG, "lst_test_inject: unknown kind %d", kind);
+  if ((kind == 1 || kind == 3) && k < 1) return fail(LST_ERR_INVALID_ARG, "lst_test_inject: k must be >= 1");
   inject().k.store(k);
   inject().kind.store(kind);
   return LST_OK;

@@ -34,7 +34,16 @@ namespace lst {
 
 // ---- the kernel -------------------------------------------------------------
 
-template <int FMT, bool SGD>
+// How a warp keeps memory busy while it works through the division and
+// square-root chain of its elements (chosen per format by measurement, see
+// launch below):
+//   SCHED_ONE       one task (2 quads per lane) loaded, computed, stored;
+//   SCHED_TWO       two tasks loaded together, then computed and stored;
+//   SCHED_PREFETCH  the next task's loads are issued before the current task
+//                   is computed and stored (register double-buffering).
+enum { SCHED_ONE = 0, SCHED_TWO = 1, SCHED_PREFETCH = 2 };
+
+template <int FMT, bool SGD, int SCHED>
 __global__ void __launch_bounds__(kThreads) lst_update_kernel(const __grid_constant__ RunTable tab,
                                                               const Scalars s) {
   const int lane = threadIdx.x & 31;
@@ -46,13 +55,51 @@ __global__ void __launch_bounds__(kThreads) lst_update_kernel(const __grid_const
     // (first_task + j) mod n_warps.
     long long j = (warp - R.first_task) % n_warps;
     if (j < 0) j += n_warps;
-    for (; j < R.tasks; j += n_warps) {
-      const long long e = j * 256 + lane * 4;
+    if (SCHED == SCHED_PREFETCH) {
+      if (j >= R.tasks) continue;
       Quad<FMT, SGD> a, b;
+      long long e = j * 256 + lane * 4;
       load_quad<FMT, SGD>(R, e, a);
       load_quad<FMT, SGD>(R, e + 128, b);
-      update_store_quad<FMT, SGD>(R, e, a, s);
-      update_store_quad<FMT, SGD>(R, e + 128, b, s);
+      for (;;) {
+        const long long jn = j + n_warps;
+        const long long en = jn * 256 + lane * 4;
+        Quad<FMT, SGD> na, nb;
+        if (jn < R.tasks) {
+          load_quad<FMT, SGD>(R, en, na);
+          load_quad<FMT, SGD>(R, en + 128, nb);
+        }
+        update_store_quad<FMT, SGD>(R, e, a, s);
+        update_store_quad<FMT, SGD>(R, e + 128, b, s);
+        if (jn >= R.tasks) break;
+        a = na;
+        b = nb;
+        e = en;
+        j = jn;
+      }
+    } else {
+      constexpr int T = (SCHED == SCHED_TWO) ? 2 : 1;
+      for (; j < R.tasks; j += T * n_warps) {
+        Quad<FMT, SGD> q[2 * T];
+#pragma unroll
+        for (int k = 0; k < T; ++k) {
+          const long long jj = j + k * n_warps;
+          if (jj < R.tasks) {
+            const long long e = jj * 256 + lane * 4;
+            load_quad<FMT, SGD>(R, e, q[2 * k]);
+            load_quad<FMT, SGD>(R, e + 128, q[2 * k + 1]);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < T; ++k) {
+          const long long jj = j + k * n_warps;
+          if (jj < R.tasks) {
+            const long long e = jj * 256 + lane * 4;
+            update_store_quad<FMT, SGD>(R, e, q[2 * k], s);
+            update_store_quad<FMT, SGD>(R, e + 128, q[2 * k + 1], s);
+          }
+        }
+      }
     }
   }
 }
@@ -61,13 +108,24 @@ __global__ void __launch_bounds__(kThreads) lst_update_kernel(const __grid_const
 
 typedef void (*KernelFn)(const RunTable, const Scalars);
 
+// Per format, the schedule and grid that measured fastest on GB300 (1.1 G
+// elements, median of 10 launches, fraction of the measured HBM copy
+// bandwidth): L16M prefetch 0.987 (one task 0.936); L16F two tasks 0.982-0.987
+// (one task 0.940); L12 one task 0.943 (two tasks 0.81, prefetch 0.84 at 256
+// threads: fewer resident warps leave memory idle through the longer compute
+// per byte of the 12 B layout). A grid of twice the resident CTAs measured
+// equal or better for every format.
 static KernelFn kernel_for(lst_format fmt, bool sgd) {
   switch (fmt) {
-    case LST_L12_BF16: return sgd ? lst_update_kernel<F_L12, true> : lst_update_kernel<F_L12, false>;
-    case LST_L16_MIXED: return sgd ? lst_update_kernel<F_L16M, true> : lst_update_kernel<F_L16M, false>;
-    default: return sgd ? lst_update_kernel<F_L16F, true> : lst_update_kernel<F_L16F, false>;
+    case LST_L12_BF16:
+      return sgd ? lst_update_kernel<F_L12, true, SCHED_ONE> : lst_update_kernel<F_L12, false, SCHED_ONE>;
+    case LST_L16_MIXED:
+      return sgd ? lst_update_kernel<F_L16M, true, SCHED_ONE> : lst_update_kernel<F_L16M, false, SCHED_PREFETCH>;
+    default:
+      return sgd ? lst_update_kernel<F_L16F, true, SCHED_ONE> : lst_update_kernel<F_L16F, false, SCHED_TWO>;
   }
 }
+constexpr int kGridPerResident = 2;
 
 // Resident CTAs per SM for each kernel instantiation, and SM count, per device.
 struct DeviceInfo {
@@ -96,7 +154,7 @@ static cudaError_t resident_ctas(lst_format fmt, bool sgd, int* total) {
     if (err != cudaSuccess) return err;
     d.ctas_per_sm[slot] = n > 0 ? n : 1;
   }
-  *total = d.sms * d.ctas_per_sm[slot];
+  *total = d.sms * d.ctas_per_sm[slot] * (sgd ? 1 : kGridPerResident);
   return cudaSuccess;
 }
 

@@ -142,7 +142,8 @@ static void drain(Engine* e) {
 using namespace lst;
 
 static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, void* dev_buf0, void* dev_buf1,
-                              const lst_adamw_hparams* hp, const lst_step_options* opts, int64_t timeout_ms) {
+                              const lst_adamw_hparams* hp, const lst_step_options* opts,
+                              const void* const* dev_grads, int64_t timeout_ms) {
   if (!Lc) return fail(LST_ERR_INVALID_ARG, "lst_stream_step: null layout");
   if (!hp) return fail(LST_ERR_INVALID_ARG, "lst_stream_step: null hparams");
   Scalars s;
@@ -170,6 +171,15 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
       return fail(LST_ERR_INVALID_ARG, "lst_stream_step: host block %lld is null", (long long)i);
     if (reinterpret_cast<uintptr_t>(host_blocks[i]) % 4096)
       return fail(LST_ERR_ALIGNMENT, "lst_stream_step: host block %lld not 4096-byte aligned", (long long)i);
+  }
+  if (dev_grads) {
+    for (int64_t i = 0; i < n; ++i) {
+      if (L->blocks[(size_t)i].bytes == 0 || skipped(i)) continue;
+      if (!dev_grads[i])
+        return fail(LST_ERR_INVALID_ARG, "lst_stream_step: gradient of block %lld is null", (long long)i);
+      if (reinterpret_cast<uintptr_t>(dev_grads[i]) % 16)
+        return fail(LST_ERR_ALIGNMENT, "lst_stream_step: gradient of block %lld not 16-byte aligned", (long long)i);
+    }
   }
   // Pinned / device checks (host-side driver queries, no device work).
   for (int64_t i = 0; i < n; ++i) {
@@ -246,12 +256,15 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
     const bool whole = (C == b.padded);
     for (int64_t e0 = 0; e0 < b.padded; e0 += C) {
       const int64_t e1 = (e0 + C < b.padded) ? e0 + C : b.padded;
-      // StreamIn: the fields the update reads.
+      // StreamIn: the fields the update reads (all but G when the gradient is
+      // already on the device; G is the first segment, so the rest is one range).
+      const int first_in = dev_grads ? 1 : 0;
       if (whole) {
-        CopyOp c{buf + b.h2d_off, host + b.h2d_off, (size_t)b.h2d_bytes, cudaMemcpyHostToDevice, E->h2d};
+        const int64_t off = b.seg_off[fi.field[first_in]];
+        CopyOp c{buf + off, host + off, (size_t)(b.h2d_off + b.h2d_bytes - off), cudaMemcpyHostToDevice, E->h2d};
         if ((err = enq(do_copy, &c)) != cudaSuccess) { what = "copy in"; break; }
       } else {
-        for (int k = 0; k < fi.n_inputs && !what; ++k) {
+        for (int k = first_in; k < fi.n_inputs && !what; ++k) {
           const int64_t off = b.seg_off[fi.field[k]] + e0 * fi.elem_bytes[k];
           CopyOp c{buf + off, host + off, (size_t)((e1 - e0) * fi.elem_bytes[k]), cudaMemcpyHostToDevice,
                    E->h2d};
@@ -265,6 +278,8 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
       if ((err = enq(do_wait, &w1)) != cudaSuccess) { what = "wait weights-ready"; break; }
       // The update on the staged chunk.
       LaunchOp l{L->fmt, block_run(*L, b, buf, e0, e1), &s, E->compute, ex, {}, nullptr, nullptr};
+      if (dev_grads)  // the update reads G from the caller's device gradient
+        l.run.g = static_cast<const char*>(dev_grads[i]) + e0 * fi.elem_bytes[0];
       if (ex) {
         l.run_ex = RunEx{l.run, bc1[(size_t)i], bc2[(size_t)i], want_sq ? (int32_t)i : -1, e0 > 0 ? 1 : 0};
         l.workspace = want_sq ? opts->workspace : nullptr;
@@ -327,12 +342,22 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
 extern "C" lst_status lst_stream_step(const lst_layout* L, void* const* host_blocks, void* dev_buf0, void* dev_buf1,
                                       const lst_adamw_hparams* hp, int64_t timeout_ms) {
   clear_error();
-  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, nullptr, timeout_ms);
+  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, nullptr, nullptr, timeout_ms);
 }
 
 extern "C" lst_status lst_stream_step_ex(const lst_layout* L, void* const* host_blocks, void* dev_buf0,
                                          void* dev_buf1, const lst_adamw_hparams* hp, const lst_step_options* opts,
                                          int64_t timeout_ms) {
   clear_error();
-  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, opts, timeout_ms);
+  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, opts, nullptr, timeout_ms);
+}
+
+extern "C" lst_status lst_stream_step_devgrad(const lst_layout* L, void* const* host_blocks,
+                                              const void* const* dev_grads, void* dev_buf0, void* dev_buf1,
+                                              const lst_adamw_hparams* hp, const lst_step_options* opts,
+                                              int64_t timeout_ms) {
+  clear_error();
+  if (L && !L->blocks.empty() && !dev_grads)
+    return fail(LST_ERR_INVALID_ARG, "lst_stream_step_devgrad: dev_grads is null");
+  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, opts, dev_grads, timeout_ms);
 }

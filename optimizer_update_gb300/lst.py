@@ -23,6 +23,7 @@ LST_ERR_NOT_PINNED = 3
 LST_ERR_CUDA = 4
 LST_ERR_OOM = 5
 LST_ERR_TIMEOUT = 6
+LST_ERR_IO = 7
 # lst_format
 LST_L12_BF16 = 0
 LST_L16_MIXED = 1
@@ -107,9 +108,18 @@ def lib() -> ctypes.CDLL:
             "lst_stream_step_ex": ([vp, P(vp), vp, vp, P(lst_adamw_hparams), P(lst_step_options), i64],
                                    ctypes.c_int),
             "lst_workspace_bytes": ([], i64),
+            "lst_stream_step_devgrad": ([vp, P(vp), P(vp), vp, vp, P(lst_adamw_hparams), P(lst_step_options), i64],
+                                        ctypes.c_int),
             "lst_adamw_step_ex_noalloc": ([vp, P(vp), P(lst_adamw_hparams), vp, vp, vp, vp], ctypes.c_int),
             "lst_host_alloc": ([i64, P(vp)], ctypes.c_int),
             "lst_host_free": ([vp], ctypes.c_int),
+            "lst_store_create": ([vp, ctypes.c_char_p, P(vp), i64, P(vp)], ctypes.c_int),
+            "lst_store_open": ([vp, ctypes.c_char_p, P(vp)], ctypes.c_int),
+            "lst_store_close": ([vp], None),
+            "lst_store_block_step": ([vp, i64, P(i64)], ctypes.c_int),
+            "lst_store_read": ([vp, i64, vp], ctypes.c_int),
+            "lst_store_write": ([vp, i64, vp, i64], ctypes.c_int),
+            "lst_store_step": ([vp, P(vp), vp, vp, P(lst_adamw_hparams), i64], ctypes.c_int),
             "lst_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "lst_last_error": ([], ctypes.c_char_p),
             "lst_test_inject": ([i32, i64], ctypes.c_int),
@@ -241,6 +251,49 @@ def lst_stream_step_ex(handle: int, host_blocks: Sequence[int], dev_buf0: int, d
                        hparams: lst_adamw_hparams, opts=None, timeout_ms: int = 0) -> None:
     _check(lib().lst_stream_step_ex(handle, _ptr_array(host_blocks), dev_buf0, dev_buf1, ctypes.byref(hparams),
                                     ctypes.byref(opts) if opts is not None else None, timeout_ms))
+
+
+def lst_stream_step_devgrad(handle: int, host_blocks: Sequence[int], dev_grads: Sequence[int], dev_buf0: int,
+                            dev_buf1: int, hparams: lst_adamw_hparams, opts=None, timeout_ms: int = 0) -> None:
+    _check(lib().lst_stream_step_devgrad(handle, _ptr_array(host_blocks), _ptr_array(dev_grads), dev_buf0, dev_buf1,
+                                         ctypes.byref(hparams), ctypes.byref(opts) if opts is not None else None,
+                                         timeout_ms))
+
+
+def lst_store_create(layout: int, directory: str, host_blocks=None, step: int = 0) -> int:
+    out = ctypes.c_void_p()
+    hb = _ptr_array(host_blocks) if host_blocks is not None else None
+    _check(lib().lst_store_create(layout, directory.encode(), hb, step, ctypes.byref(out)))
+    return out.value
+
+
+def lst_store_open(layout: int, directory: str) -> int:
+    out = ctypes.c_void_p()
+    _check(lib().lst_store_open(layout, directory.encode(), ctypes.byref(out)))
+    return out.value
+
+
+def lst_store_close(store: int) -> None:
+    lib().lst_store_close(store)
+
+
+def lst_store_block_step(store: int, layer: int) -> int:
+    v = ctypes.c_int64()
+    _check(lib().lst_store_block_step(store, layer, ctypes.byref(v)))
+    return v.value
+
+
+def lst_store_read(store: int, layer: int, host_dst: int) -> None:
+    _check(lib().lst_store_read(store, layer, host_dst))
+
+
+def lst_store_write(store: int, layer: int, host_src: int, step: int) -> None:
+    _check(lib().lst_store_write(store, layer, host_src, step))
+
+
+def lst_store_step(store: int, staging: Sequence[int], dev_buf0: int, dev_buf1: int, hparams: lst_adamw_hparams,
+                   timeout_ms: int = 0) -> None:
+    _check(lib().lst_store_step(store, _ptr_array(staging), dev_buf0, dev_buf1, ctypes.byref(hparams), timeout_ms))
 
 
 def lst_host_alloc(nbytes: int) -> int:

@@ -253,3 +253,58 @@ def test_zero_copy_rejects_pageable_and_device_memory():
     with pytest.raises(lst.LstError) as e:
         lst.lst_zero_copy_step(L.handle, [x.data_ptr() for x in d], lst.adamw_hparams(), 0)
     assert e.value.status == lst.LST_ERR_NOT_PINNED
+
+
+# ---- gradients already on the device: only the state crosses the link inbound ----
+@pytest.mark.parametrize("fmt,workload", FMTS)
+@pytest.mark.parametrize("chunk", [0, 1 << 20])
+def test_stream_devgrad_bit_identical(fmt, workload, chunk):
+    L = Layout(_three_tinyllama_layers(), fmt)
+    L.set_stream_chunk(chunk)
+    P = PinnedBlocks(L)
+    try:
+        for i in range(L.n_layers):
+            fill_host_block(L, i, P.arrays[i], workload, 10)
+        dev = [torch.from_numpy(P.arrays[i].copy()).cuda() for i in range(L.n_layers)]
+        grads = [torch.from_numpy(L.numpy_views(i, P.arrays[i])["G"].copy().view(np.uint8)).cuda()
+                 for i in range(L.n_layers)]
+        # the host G segments now hold something else: they must be neither read nor written
+        poison = []
+        for i in range(L.n_layers):
+            g = L.numpy_views(i, P.arrays[i])["G"].view(np.uint8)
+            g[:] = 0x7F
+            poison.append(g.copy())
+        b0, b1 = _bufs(L)
+        for k in range(2):
+            hp, _ = hparams_for(workload, 10 + k)
+            lst.lst_adamw_step(L.handle, [d.data_ptr() for d in dev], hp, torch.cuda.current_stream().cuda_stream)
+            torch.cuda.synchronize()
+            lst.lst_stream_step_devgrad(L.handle, P.ptrs, [g.data_ptr() for g in grads], b0.data_ptr(),
+                                        b1.data_ptr(), hp, None, 600_000)
+        for i in range(L.n_layers):
+            got, exp = L.numpy_views(i, P.arrays[i]), L.numpy_views(i, dev[i].cpu().numpy())
+            for f in got:
+                if f == "G":
+                    assert np.array_equal(got[f].view(np.uint8), poison[i])
+                else:
+                    assert np.array_equal(got[f].view(np.uint8), exp[f].view(np.uint8)), (i, f)
+    finally:
+        P.free()
+
+
+def test_stream_devgrad_validation():
+    L = _small()
+    P = PinnedBlocks(L)
+    try:
+        b0, b1 = _bufs(L)
+        with pytest.raises(lst.LstError) as e:
+            lst.lst_stream_step_devgrad(L.handle, P.ptrs, [0] * L.n_layers, b0.data_ptr(), b1.data_ptr(),
+                                        lst.adamw_hparams(), None, 10_000)
+        assert e.value.status == lst.LST_ERR_INVALID_ARG
+        g = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+        with pytest.raises(lst.LstError) as e:
+            lst.lst_stream_step_devgrad(L.handle, P.ptrs, [g.data_ptr() + 8] * L.n_layers, b0.data_ptr(),
+                                        b1.data_ptr(), lst.adamw_hparams(), None, 10_000)
+        assert e.value.status == lst.LST_ERR_ALIGNMENT
+    finally:
+        P.free()
