@@ -308,3 +308,29 @@ def test_stream_devgrad_validation():
         assert e.value.status == lst.LST_ERR_ALIGNMENT
     finally:
         P.free()
+
+
+@pytest.mark.slow
+def test_stream_llama7b_full_bit_identical_to_device():
+    """LLaMA-7B, 12 B/param, 34 blocks (80.9 GB): the same step device-resident
+    and streamed from pinned host memory give the same bytes everywhere."""
+    workload, fmt = "llama7b_l12", "L12"
+    L = Layout(shapes.llama7b(), fmt)
+    P = PinnedBlocks(L)
+    try:
+        for i in range(L.n_layers):
+            fill_host_block(L, i, P.arrays[i], workload, 10)
+        dev = []
+        for i in range(L.n_layers):
+            d = torch.empty(L.block_bytes(i), dtype=torch.uint8, device="cuda")
+            d.copy_(torch.from_numpy(P.arrays[i]))
+            dev.append(d)
+        hp, _ = hparams_for(workload, 10)
+        lst.lst_adamw_step(L.handle, [d.data_ptr() for d in dev], hp, torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        b0, b1 = _bufs(L)
+        lst.lst_stream_step(L.handle, P.ptrs, b0.data_ptr(), b1.data_ptr(), hp, 600_000)
+        for i in range(L.n_layers):
+            assert torch.equal(dev[i], torch.from_numpy(P.arrays[i]).cuda()), f"block {i}"
+    finally:
+        P.free()
