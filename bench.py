@@ -32,6 +32,7 @@ ranks of parameters updated divided by the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -259,8 +260,13 @@ def run_reference(args):
     arrs, blocks, budget_params = [], [], None
     # size the sample so one step takes about --ref-step-s seconds
     i = 0
-    while i < L.n_layers:
+    # The sample is also bounded in memory (about 2 GiB of state), so that the
+    # reference run leaves the host's free memory much as it found it for the
+    # run measured after it.
+    state = 0
+    while i < L.n_layers and (state == 0 or state + L.block_bytes(i) <= (2 << 30)):
         a = np.empty(L.block_bytes(i), np.uint8)
+        state += L.block_bytes(i)
         synth.fill_block(L.numpy_views(i, a), L.spans(i), i, args.workload, L.fmt, t=1, seed=args.seed)
         t0 = time.perf_counter()
         oracle.step(L.fmt, L.numpy_views(i, a), oracle.hparams(step=1, **hp_kw), threads=threads)
@@ -391,13 +397,20 @@ def run_ours(args):
     torch.cuda.synchronize(device)
     barrier(device)
     torch.cuda.synchronize(device)
+    # arguments marshalled once: the host enqueues each launch with one C call
+    ptr_arr = lst._ptr_array(dptrs)
+    hp = lst.adamw_hparams(step=t, **hp_kw)
+    call = lst.lib().lst_adamw_step
     for k in range(args.steps):
         if flush is not None:
             with torch.cuda.stream(stream):
                 flush.fill_(k & 0xFF)
                 flush_rd.sum()
         starts[k].record(stream)
-        lst.lst_adamw_step(L.handle, dptrs, lst.adamw_hparams(step=t, **hp_kw), stream.cuda_stream)
+        hp.step = t
+        st = call(L.handle, ptr_arr, ctypes.byref(hp), stream.cuda_stream)
+        if st != lst.LST_OK:
+            raise lst.LstError(st, lst.lst_last_error())
         t += 1
         ends[k].record(stream)
     torch.cuda.synchronize(device)
@@ -534,7 +547,8 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": f"lst_update_kernel<{L.fmt}>", "alg_bytes_per_launch": alg_bytes,
-                         "avg_launch_ms": 1e3 * avg_launch, "peak_source": f"{peak_kind} hbm_gbs"},
+                         "avg_launch_ms": 1e3 * avg_launch, "median_launch_ms": 1e3 * statistics.median(per_launch),
+                         "min_launch_ms": 1e3 * min(per_launch), "peak_source": f"{peak_kind} hbm_gbs"},
             "e2e": {"value": e2e_value, "unit": "params/s", "h2d_bytes_per_step": h2d_b,
                     "d2h_bytes_per_step": d2h_b, "steps": e_steps, "call": "lst_stream_step",
                     "gpu_launches": e_steps * chunks},

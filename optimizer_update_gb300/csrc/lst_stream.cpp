@@ -156,7 +156,9 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
     lst_status st = prepare_options(L, *hp, opts, &bc1, &bc2, "lst_stream_step");
     if (st != LST_OK) return st;
   }
-  const bool ex = opts != nullptr;
+  // The extended kernel is needed for per-block bias corrections or sums of
+  // squares; a skip mask alone only changes which chunks are launched.
+  const bool ex = opts != nullptr && (opts->block_steps != nullptr || opts->grad_sq != nullptr);
   const bool want_sq = opts && opts->grad_sq;
   auto skipped = [&](int64_t i) { return opts && opts->skip && opts->skip[i]; };
   const int64_t n = (int64_t)L->blocks.size();
