@@ -43,16 +43,19 @@ namespace lst {
 //                   is computed and stored (register double-buffering).
 enum { SCHED_ONE = 0, SCHED_TWO = 1, SCHED_PREFETCH = 2 };
 
+// Large launches: each warp walks its tasks run by run (task j of a run is
+// global task first_task + j, owned by warp (first_task + j) mod n_warps).
+// Every run spans many tasks per warp, so the schedule overlaps tasks inside
+// a run and the run's entry stays in registers for the whole loop.
 template <int FMT, bool SGD, int SCHED>
 __global__ void __launch_bounds__(kThreads) lst_update_kernel(const __grid_constant__ RunTable tab,
-                                                              const Scalars s) {
+                                                              const Scalars s, const long long total_tasks) {
+  (void)total_tasks;
   const int lane = threadIdx.x & 31;
   const long long n_warps = (long long)gridDim.x * (kThreads / 32);
   const long long warp = (long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
   for (int r = 0; r < tab.n; ++r) {
     const RunTable::Entry& R = tab.r[r];
-    // Task j of this run is global task first_task + j, owned by warp
-    // (first_task + j) mod n_warps.
     long long j = (warp - R.first_task) % n_warps;
     if (j < 0) j += n_warps;
     if (SCHED == SCHED_PREFETCH) {
@@ -104,9 +107,56 @@ __global__ void __launch_bounds__(kThreads) lst_update_kernel(const __grid_const
   }
 }
 
+// A warp's position in the run table, held in registers: the run holding
+// the current task and a copy of its entry. Tasks of a warp only increase,
+// so the cursor only moves forward, and it reads the table only when a task
+// falls past the end of the run it holds.
+struct Cursor {
+  int r;
+  long long end;  // first global task after run r
+  RunTable::Entry R;
+};
+
+__device__ __forceinline__ void cursor_seek(const RunTable& tab, long long g, Cursor& c) {
+  if (g < c.end) return;
+  int r = c.r;
+  while (r < tab.n && g >= tab.r[r].first_task + tab.r[r].tasks) ++r;
+  c.r = r;
+  if (r < tab.n) {
+    c.R = tab.r[r];
+    c.end = c.R.first_task + c.R.tasks;
+  }
+}
+
+// Small launches (many small runs, few tasks per warp, e.g. 22 LoRA blocks):
+// each warp walks its global tasks g = warp, warp + n_warps, ... across run
+// boundaries with a cursor, one task at a time, with as many resident warps as
+// 64 registers allow (4 CTAs of 256 threads per SM): at this size the writes
+// stay in L2 and the latency of the division chains, not HBM, sets the pace.
+template <int FMT, bool SGD>
+__global__ void __launch_bounds__(kThreads, 4) lst_update_small_kernel(const __grid_constant__ RunTable tab,
+                                                                      const Scalars s, const long long total_tasks) {
+  const int lane = threadIdx.x & 31;
+  const long long n_warps = (long long)gridDim.x * (kThreads / 32);
+  long long g = (long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  if (g >= total_tasks) return;
+  Cursor cur;
+  cur.r = 0;
+  cur.end = 0;
+  for (; g < total_tasks; g += n_warps) {
+    cursor_seek(tab, g, cur);
+    const long long e = (g - cur.R.first_task) * 256 + lane * 4;
+    Quad<FMT, SGD> a, b;
+    load_quad<FMT, SGD>(cur.R, e, a);
+    load_quad<FMT, SGD>(cur.R, e + 128, b);
+    update_store_quad<FMT, SGD>(cur.R, e, a, s);
+    update_store_quad<FMT, SGD>(cur.R, e + 128, b, s);
+  }
+}
+
 // ---- launch -----------------------------------------------------------------
 
-typedef void (*KernelFn)(const RunTable, const Scalars);
+typedef void (*KernelFn)(const RunTable, const Scalars, const long long);
 
 // Per format, the schedule and grid that measured fastest on GB300 (1.1 G
 // elements, median of 10 launches, fraction of the measured HBM copy
@@ -115,7 +165,14 @@ typedef void (*KernelFn)(const RunTable, const Scalars);
 // threads: fewer resident warps leave memory idle through the longer compute
 // per byte of the 12 B layout). A grid of twice the resident CTAs measured
 // equal or better for every format.
-static KernelFn kernel_for(lst_format fmt, bool sgd) {
+static KernelFn kernel_for(lst_format fmt, bool sgd, bool small) {
+  if (small) {
+    switch (fmt) {
+      case LST_L12_BF16: return sgd ? lst_update_small_kernel<F_L12, true> : lst_update_small_kernel<F_L12, false>;
+      case LST_L16_MIXED: return sgd ? lst_update_small_kernel<F_L16M, true> : lst_update_small_kernel<F_L16M, false>;
+      default: return sgd ? lst_update_small_kernel<F_L16F, true> : lst_update_small_kernel<F_L16F, false>;
+    }
+  }
   switch (fmt) {
     case LST_L12_BF16:
       return sgd ? lst_update_kernel<F_L12, true, SCHED_ONE> : lst_update_kernel<F_L12, false, SCHED_ONE>;
@@ -125,23 +182,27 @@ static KernelFn kernel_for(lst_format fmt, bool sgd) {
       return sgd ? lst_update_kernel<F_L16F, true, SCHED_ONE> : lst_update_kernel<F_L16F, false, SCHED_TWO>;
   }
 }
+// A launch moving less than this many algorithmic bytes is not HBM-bound: its
+// writes stay in L2 and its reads take a few microseconds, so the latency of
+// the fp32 division chains dominates; it uses lst_update_small_kernel.
+constexpr long long kSmallLaunchBytes = 512ll << 20;
 constexpr int kGridPerResident = 2;
 
 // Resident CTAs per SM for each kernel instantiation, and SM count, per device.
 struct DeviceInfo {
   int sms = 0;
-  int ctas_per_sm[6] = {0, 0, 0, 0, 0, 0};
+  int ctas_per_sm[12] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 };
 constexpr int kMaxDevices = 64;
 static DeviceInfo g_dev[kMaxDevices];
 static std::mutex g_dev_mu;
 
-static cudaError_t resident_ctas(lst_format fmt, bool sgd, int* total) {
+static cudaError_t resident_ctas(lst_format fmt, bool sgd, bool small, int* total) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  const int slot = (int)fmt * 2 + (sgd ? 1 : 0);
+  const int slot = (int)fmt * 4 + (sgd ? 2 : 0) + (small ? 1 : 0);
   std::lock_guard<std::mutex> g(g_dev_mu);
   DeviceInfo& d = g_dev[dev];
   if (d.sms == 0) {
@@ -150,7 +211,7 @@ static cudaError_t resident_ctas(lst_format fmt, bool sgd, int* total) {
   }
   if (d.ctas_per_sm[slot] == 0) {
     int n = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_for(fmt, sgd), kThreads, 0);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_for(fmt, sgd, small), kThreads, 0);
     if (err != cudaSuccess) return err;
     d.ctas_per_sm[slot] = n > 0 ? n : 1;
   }
@@ -160,10 +221,7 @@ static cudaError_t resident_ctas(lst_format fmt, bool sgd, int* total) {
 
 cudaError_t launch_update(lst_format fmt, bool sgd, const Run* runs, int n_runs, const Scalars& s,
                           cudaStream_t stream) {
-  int max_ctas = 0;
-  cudaError_t err = resident_ctas(fmt, sgd, &max_ctas);
-  if (err != cudaSuccess) return err;
-  KernelFn fn = kernel_for(fmt, sgd);
+  const FormatInfo& fi = format_info(fmt);
   int i = 0;
   while (i < n_runs) {
     RunTable tab;
@@ -184,10 +242,16 @@ cudaError_t launch_update(lst_format fmt, bool sgd, const Run* runs, int n_runs,
       tasks += e.tasks;
     }
     if (tab.n == 0) continue;
+    // algorithmic bytes of the launch: reads and writes of every element
+    const long long bytes = tasks * kWarpSpan * (long long)(fi.bytes_per_param + (fmt == LST_L12_BF16 ? 10 : 12));
+    const bool small = bytes < kSmallLaunchBytes;
+    int max_ctas = 0;
+    cudaError_t err = resident_ctas(fmt, sgd, small, &max_ctas);
+    if (err != cudaSuccess) return err;
     const long long warps_per_cta = kThreads / 32;
     long long grid = (tasks + warps_per_cta - 1) / warps_per_cta;
     if (grid > max_ctas) grid = max_ctas;
-    fn<<<(unsigned)grid, kThreads, 0, stream>>>(tab, s);
+    kernel_for(fmt, sgd, small)<<<(unsigned)grid, kThreads, 0, stream>>>(tab, s, tasks);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
