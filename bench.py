@@ -173,10 +173,13 @@ def measured_peaks():
 
 
 def kernel_source_sha() -> str:
-    """Hash of the sources of the device-resident update kernel."""
+    """Hash of the device code of the update kernels: lst_device.cuh and the
+    part of lst_kernels.cu before its host-side launch section."""
+    csrc = os.path.join(ROOT, "optimizer_update_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("lst_device.cuh", "lst_kernels.cu"):
-        h.update(open(os.path.join(ROOT, "optimizer_update_gb300", "csrc", f), "rb").read())
+    h.update(open(os.path.join(csrc, "lst_device.cuh"), "rb").read())
+    k = open(os.path.join(csrc, "lst_kernels.cu"), "rb").read()
+    h.update(k.split(b"// ---- launch ----")[0])
     return h.hexdigest()[:16]
 
 

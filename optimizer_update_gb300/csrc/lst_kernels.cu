@@ -185,7 +185,7 @@ static KernelFn kernel_for(lst_format fmt, bool sgd, bool small) {
 // A launch moving less than this many algorithmic bytes is not HBM-bound: its
 // writes stay in L2 and its reads take a few microseconds, so the latency of
 // the fp32 division chains dominates; it uses lst_update_small_kernel.
-constexpr long long kSmallLaunchBytes = 512ll << 20;
+constexpr long long kSmallLaunchBytes = 256ll << 20;  // about twice the L2
 constexpr int kGridPerResident = 2;
 
 // Resident CTAs per SM for each kernel instantiation, and SM count, per device.
