@@ -22,6 +22,7 @@
 #include <chrono>
 #include <new>
 #include <thread>
+#include <vector>
 
 #include "lst_internal.h"
 
@@ -131,6 +132,43 @@ static cudaError_t do_launch(void* p) {
   return launch_update(l->fmt, false, &l->run, 1, *l->s, l->st);
 }
 
+// Chunk boundaries of one block: chunks of C elements, except that the
+// step's first block starts with chunks of C/8, C/4, C/2 and its last block
+// ends with C/2, C/4, C/8, so that the pipeline fills (first inbound copy
+// before any update) and drains (last outbound copy after the last update) in
+// a small chunk rather than a full one. Every boundary stays a multiple of
+// 2048 elements.
+static std::vector<int64_t> chunk_cuts(int64_t padded, int64_t C, bool first_block, bool last_block) {
+  std::vector<int64_t> sizes;
+  if (C >= padded) {
+    sizes.push_back(padded);
+  } else {
+    int64_t left = padded;
+    std::vector<int64_t> head, tail;
+    for (int64_t k = 8; k >= 2; k /= 2) {  // C/8, C/4, C/2
+      const int64_t c = (C / k) / kBlockAlign * kBlockAlign;
+      if (first_block && c > 0 && left > C + c) {
+        head.push_back(c);
+        left -= c;
+      }
+      if (last_block && c > 0 && left > C + c) {
+        tail.push_back(c);
+        left -= c;
+      }
+    }
+    sizes = head;
+    while (left > 0) {
+      const int64_t c = left < C ? left : C;
+      sizes.push_back(c);
+      left -= c;
+    }
+    sizes.insert(sizes.end(), tail.rbegin(), tail.rend());
+  }
+  std::vector<int64_t> cuts(1, 0);
+  for (int64_t c : sizes) cuts.push_back(cuts.back() + c);
+  return cuts;
+}
+
 static void drain(Engine* e) {
   cudaStreamSynchronize(e->h2d);
   cudaStreamSynchronize(e->compute);
@@ -234,6 +272,12 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
   bool used[2] = {false, false};
   const char* what = nullptr;
 
+  int64_t first_active = -1, last_active = -1;
+  for (int64_t i = 0; i < n; ++i) {
+    if (skipped(i) || L->blocks[(size_t)i].padded == 0) continue;
+    if (first_active < 0) first_active = i;
+    last_active = i;
+  }
   for (int64_t i = 0; i < n && !what; ++i) {
     const Block& b = L->blocks[(size_t)i];
     if (skipped(i)) continue;  // a locked block: no transfer, no update
@@ -256,8 +300,9 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
     used[bi] = true;
     const int64_t C = (L->stream_chunk > 0 && L->stream_chunk < b.padded) ? L->stream_chunk : b.padded;
     const bool whole = (C == b.padded);
-    for (int64_t e0 = 0; e0 < b.padded; e0 += C) {
-      const int64_t e1 = (e0 + C < b.padded) ? e0 + C : b.padded;
+    const std::vector<int64_t> cuts = chunk_cuts(b.padded, C, i == first_active, i == last_active);
+    for (size_t ci = 0; ci + 1 < cuts.size(); ++ci) {
+      const int64_t e0 = cuts[ci], e1 = cuts[ci + 1];
       // StreamIn: the fields the update reads (all but G when the gradient is
       // already on the device; G is the first segment, so the rest is one range).
       const int first_in = dev_grads ? 1 : 0;
