@@ -1,0 +1,73 @@
+"""The boundary is plain C: a C99 program includes include/lst.h, links
+liblst.so and drives the host-only calls (no GPU needed)."""
+
+import os
+import shutil
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "lst.h"
+
+int main(void) {
+  /* two blocks: a 4x8 weight and a norm in block 0, a 1000-element tensor in block 1 */
+  int32_t ndim[3] = {2, 1, 1};
+  int64_t dims[12] = {4, 8, 0, 0, 8, 0, 0, 0, 1000, 0, 0, 0};
+  int32_t layer[3] = {0, 0, 1};
+  lst_layout* L = NULL;
+  lst_status st = lst_layout_create(3, ndim, dims, layer, LST_L16_MIXED, &L);
+  if (st != LST_OK) { printf("create: %s\n", lst_status_string(st)); return 1; }
+  int64_t n_layers = 0, n_params = 0, max_bytes = 0;
+  lst_layout_info(L, &n_layers, &n_params, &max_bytes);
+  int64_t bytes = 0, params = 0, padded = 0, off = 0, seg = 0;
+  lst_layout_block(L, 1, &bytes, &params, &padded);
+  lst_layout_segment(L, 1, LST_FIELD_W, &off, &seg);
+  int64_t t_off = 0, t_layer = 0, t_elem = 0;
+  lst_layout_tensor(L, 1, LST_FIELD_MASTER, &t_off, &t_layer, &t_elem);
+  printf("%lld %lld %lld %lld %lld %lld %lld %lld %lld %lld\n", (long long)n_layers, (long long)n_params,
+         (long long)max_bytes, (long long)bytes, (long long)params, (long long)padded, (long long)off,
+         (long long)seg, (long long)t_off, (long long)t_elem);
+  /* a bad step counter is refused before any CUDA call */
+  lst_adamw_hparams hp = {1e-4f, 0.9f, 0.999f, 1e-8f, 0.01f, 0};
+  void* blocks[2] = {0, 0};
+  st = lst_adamw_step(L, blocks, &hp, NULL);
+  printf("%d %s | %s\n", (int)st, lst_status_string(st), lst_last_error());
+  lst_layout_destroy(L);
+  return 0;
+}
+"""
+
+
+@pytest.fixture(scope="module")
+def libdir():
+    from optimizer_update_gb300 import lst
+    if not os.path.exists(lst.LIB_PATH):
+        from optimizer_update_gb300 import build
+        build.build()
+    return os.path.dirname(lst.LIB_PATH)
+
+
+def test_c99_program_uses_the_abi(libdir, tmp_path):
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_lst.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_lst"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-L", libdir, "-llst", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    nums = [int(x) for x in out[0].split()]
+    # block 0: 32 + 8 params, block 1: 1000 params; each padded to 2048 elements
+    assert nums[:3] == [2, 1040, 16 * 2048]
+    assert nums[3:6] == [16 * 2048, 1000, 2048]
+    assert nums[6:8] == [14 * 2048, 2 * 2048]        # W is the last segment of the mixed layout
+    # tensor 1 (the norm) sits after the 32-element weight in block 0: its
+    # master data starts after the bf16 G segment, 32 fp32 elements in
+    assert nums[8:10] == [2 * 2048 + 32 * 4, 32]
+    assert out[1].startswith("1 invalid argument")
