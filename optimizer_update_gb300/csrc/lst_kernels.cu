@@ -47,9 +47,18 @@ enum { SCHED_ONE = 0, SCHED_TWO = 1, SCHED_PREFETCH = 2 };
 // global task first_task + j, owned by warp (first_task + j) mod n_warps).
 // Every run spans many tasks per warp, so the schedule overlaps tasks inside
 // a run and the run's entry stays in registers for the whole loop.
+// Resident CTAs per SM the compiler must allow for: the 12 B layout's prefetch
+// schedule is held to 80 registers (3 CTAs of 256 threads per SM), where it
+// measured 0.977-0.980 of the copy bandwidth against 0.845 at 2 CTAs; the
+// 16 B layouts measured best uncapped (a cap of 80 spilled and lost 7-9 %).
+template <int FMT, int SCHED>
+struct MinCtas {
+  static constexpr int value = (FMT == F_L12 && SCHED == SCHED_PREFETCH) ? 3 : 1;
+};
+
 template <int FMT, bool SGD, int SCHED>
-__global__ void __launch_bounds__(kThreads) lst_update_kernel(const __grid_constant__ RunTable tab,
-                                                              const Scalars s, const long long total_tasks) {
+__global__ void __launch_bounds__(kThreads, (MinCtas<FMT, SCHED>::value))
+    lst_update_kernel(const __grid_constant__ RunTable tab, const Scalars s, const long long total_tasks) {
   (void)total_tasks;
   const int lane = threadIdx.x & 31;
   const long long n_warps = (long long)gridDim.x * (kThreads / 32);
@@ -160,11 +169,10 @@ typedef void (*KernelFn)(const RunTable, const Scalars, const long long);
 
 // Per format, the schedule and grid that measured fastest on GB300 (1.1 G
 // elements, median of 10 launches, fraction of the measured HBM copy
-// bandwidth): L16M prefetch 0.987 (one task 0.936); L16F two tasks 0.982-0.987
-// (one task 0.940); L12 one task 0.943 (two tasks 0.81, prefetch 0.84 at 256
-// threads: fewer resident warps leave memory idle through the longer compute
-// per byte of the 12 B layout). A grid of twice the resident CTAs measured
-// equal or better for every format.
+// bandwidth, several boxes): L16M prefetch 0.979-0.987 (one task
+// 0.936-0.940); L16F two tasks 0.964-0.987 (one task 0.940); L12 prefetch at
+// 3 CTAs per SM 0.968-0.980 (one task 0.917-0.943; two tasks 0.81). A grid of
+// twice the resident CTAs measured equal or better for every format.
 static KernelFn kernel_for(lst_format fmt, bool sgd, bool small) {
   if (small) {
     switch (fmt) {
@@ -175,7 +183,7 @@ static KernelFn kernel_for(lst_format fmt, bool sgd, bool small) {
   }
   switch (fmt) {
     case LST_L12_BF16:
-      return sgd ? lst_update_kernel<F_L12, true, SCHED_ONE> : lst_update_kernel<F_L12, false, SCHED_ONE>;
+      return sgd ? lst_update_kernel<F_L12, true, SCHED_ONE> : lst_update_kernel<F_L12, false, SCHED_PREFETCH>;
     case LST_L16_MIXED:
       return sgd ? lst_update_kernel<F_L16M, true, SCHED_ONE> : lst_update_kernel<F_L16M, false, SCHED_PREFETCH>;
     default:
