@@ -194,3 +194,57 @@ def test_tinyllama_full_l16m_sampled():
 @pytest.mark.slow
 def test_llama7b_l12_sampled():
     assert _full_size_sampled(shapes.llama7b(), "L12", "llama7b_l12", 10, 2) > 100_000
+
+
+@pytest.mark.parametrize("fmt", ["L12", "L16M", "L16F"])
+@pytest.mark.parametrize("eps", [1e-8, 0.0])
+def test_zeros_signed_zeros_and_tiny_values_bit_exact(fmt, eps):
+    """Exact zeros (in g, m, v, w), negative zeros and subnormal-range values:
+    the cases in which the kernel substitutes known IEEE results for the
+    division and square root must still match the oracle bit for bit (with
+    eps = 0 a zero moment gives 0/0 = NaN on both sides)."""
+    n = 4096 * 8
+    L = Layout([("x", (n,), 0)], fmt)
+    host = np.zeros(L.block_bytes(0), np.uint8)
+    v = L.numpy_views(0, host)
+    rng = np.random.default_rng(77)
+    kinds = rng.integers(0, 6, n)
+    def pick(scale):
+        x = (rng.standard_normal(n) * scale).astype(np.float32)
+        x[kinds == 0] = 0.0
+        x[kinds == 1] = -0.0
+        x[kinds == 2] *= np.float32(1e-36)          # subnormal-range products
+        return x
+    g32, m32 = pick(1e-3), pick(1e-4)
+    v32 = np.abs(pick(1e-6)).astype(np.float32)
+    v32[kinds == 1] = 0.0
+    w32 = pick(0.02)
+    if fmt == "L16F":
+        v["G"][:] = g32
+        v["W"][:] = w32
+    else:
+        v["G"][:] = oracle.bf16_from_f32(g32)
+        if fmt == "L12":
+            v["W"][:] = oracle.bf16_from_f32(w32)
+        else:
+            v["MASTER"][:] = w32
+    v["M"][:] = m32
+    v["V"][:] = v32
+    blk = torch.from_numpy(host).cuda()
+    hp_kw = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=eps, weight_decay=0.01, step=3)
+    lst.lst_adamw_step(L.handle, [blk.data_ptr()], lst.adamw_hparams(**hp_kw), _stream())
+    torch.cuda.synchronize()
+    oracle.step(fmt, L.numpy_views(0, host), oracle.hparams(**hp_kw))
+    got, exp = L.numpy_views(0, blk.cpu().numpy()), L.numpy_views(0, host)
+    for f in got:
+        if f == "G":
+            continue
+        if got[f].dtype == np.float32:
+            gn, en = np.isnan(got[f]), np.isnan(exp[f])
+            assert np.array_equal(gn, en), f
+            assert np.array_equal(got[f][~gn].view(np.uint32), exp[f][~en].view(np.uint32)), f
+        else:
+            gf, ef = oracle.f32_from_bf16(got[f]), oracle.f32_from_bf16(exp[f])
+            assert np.array_equal(np.isnan(gf), np.isnan(ef)), f
+            ok = ~np.isnan(ef)
+            assert np.array_equal(got[f][ok], exp[f][ok]), f
