@@ -72,9 +72,11 @@ def dist_env():
 
 
 def dist_init(backend: str):
+    """Joins the process group when launched by torchrun (any world size, so
+    the same path runs with one process as with eight)."""
     import torch.distributed as dist
     rank, _, world = dist_env()
-    if world > 1 and not dist.is_initialized():
+    if "RANK" in os.environ and "MASTER_ADDR" in os.environ and not dist.is_initialized():
         dist.init_process_group(backend=backend, rank=rank, world_size=world)
     return rank, world
 
@@ -477,7 +479,10 @@ def run_ours(args):
     e2e_value = world * P * e_steps / t_e2e_max
     chunks = sum((L.padded(i) + chunk - 1) // chunk for i in range(L.n_layers))
     roof_t = max(h2d_b / (link["h2d_concurrent_gbs"] * 1e9), d2h_b / (link["d2h_concurrent_gbs"] * 1e9))
-    stream_info = dict(link, step_ms=1e3 * t_e2e / e_steps,
+    # the same bytes with the two directions one after the other (each at its
+    # measured bandwidth alone): what the three-stream overlap saves
+    serial_t = h2d_b / (link["h2d_gbs"] * 1e9) + d2h_b / (link["d2h_gbs"] * 1e9)
+    stream_info = dict(link, step_ms=1e3 * t_e2e / e_steps, serial_copies_ms=1e3 * serial_t,
                        achieved_h2d_gbs=h2d_b * e_steps / t_e2e / 1e9,
                        achieved_d2h_gbs=d2h_b * e_steps / t_e2e / 1e9,
                        roofline_ms=1e3 * roof_t, frac_of_link_roofline=roof_t / (t_e2e / e_steps),
