@@ -58,6 +58,9 @@ WORKLOADS = {
 }
 # Algorithmic bytes per parameter of one device-resident step (reads + writes).
 ALG_BYTES = {"L12": 22, "L16M": 28, "L16F": 28}
+# algorithmic bytes below which the launch path uses lst_update_small_kernel
+# (kSmallLaunchBytes in lst_kernels.cu: about twice the 129 MB L2)
+SMALL_LAUNCH_BYTES = 256 << 20
 HP = dict(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
 HP_LORA = dict(lr=2e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
 
@@ -185,21 +188,24 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_traffic(params: int):
-    """DRAM bytes per launch of the update kernel from the committed ncu
-    summary, scaled to `params`; None if the kernel source changed since."""
+def kernel_traffic(kernel: str, fmt: str, params: int):
+    """DRAM bytes per launch of `kernel` on format `fmt` from the committed ncu
+    summary (bytes per parameter of a captured case), scaled to `params`; None
+    if that pair was not captured or the kernels' device code changed since."""
     summ = os.path.join(ROOT, "profiles", "lst_update_kernel_traffic.txt")
     if not os.path.exists(summ):
         return None
-    sha = kernel_source_sha()
-    vals = {}
+    sha, per_param = None, None
     for line in open(summ):
         p = line.split()
-        if len(p) >= 2 and not line.startswith("#"):
-            vals[p[0]] = p[1]
-    if vals.get("kernel_source_sha256_16") != sha:
+        if not p or line.startswith("#"):
+            continue
+        if p[0] == "kernel_source_sha256_16":
+            sha = p[1]
+        elif p[0] == "traffic" and p[1] == kernel and p[2] == fmt:
+            per_param = float(p[3])
+    if sha != kernel_source_sha() or per_param is None:
         return None
-    per_param = float(vals["dram_bytes_per_param"])
     return per_param * params
 
 
@@ -430,7 +436,9 @@ def run_ours(args):
     alg_bytes = ALG_BYTES[L.fmt] * P
     peak, peak_kind = measured_peaks()
     achieved = alg_bytes / avg_launch / 1e9
-    traffic = kernel_traffic(P)
+    # the launch path picks the cross-run kernel below about twice the L2
+    kname = "lst_update_small_kernel" if alg_bytes < SMALL_LAUNCH_BYTES else "lst_update_kernel"
+    traffic = kernel_traffic(kname, L.fmt, P)
     del dev
     torch.cuda.empty_cache()
 
@@ -554,7 +562,7 @@ def run_ours(args):
             "config": config_for(L, args.workload, world, args.max_blocks),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": f"lst_update_kernel<{L.fmt}>", "alg_bytes_per_launch": alg_bytes,
+                         "kernel": f"{kname}<{L.fmt}>", "alg_bytes_per_launch": alg_bytes,
                          "avg_launch_ms": 1e3 * avg_launch, "median_launch_ms": 1e3 * statistics.median(per_launch),
                          "min_launch_ms": 1e3 * min(per_launch), "peak_source": f"{peak_kind} hbm_gbs"},
             "e2e": {"value": e2e_value, "unit": "params/s", "h2d_bytes_per_step": h2d_b,
