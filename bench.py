@@ -439,6 +439,10 @@ def run_ours(args):
     # the launch path picks the cross-run kernel below about twice the L2
     kname = "lst_update_small_kernel" if alg_bytes < SMALL_LAUNCH_BYTES else "lst_update_kernel"
     traffic = kernel_traffic(kname, L.fmt, P)
+    # ---- per-block options leg: lst_adamw_step_ex with a step counter per
+    # block (staggered, as after progressive locking) and every block's
+    # sum of g^2 returned by the same pass ---------------------------------------
+    options = time_options_leg(args, L, dptrs, hp_kw, stream, device, world, t, flush, flush_rd, peak)
     del dev
     torch.cuda.empty_cache()
 
@@ -543,6 +547,11 @@ def run_ours(args):
                  "step_ms": 1e3 * t_zc / e_steps, "link_bytes_per_step": h2d_b + d2h_b,
                  "frac_of_link_roofline": roof_t / (t_zc / e_steps), "steps": e_steps, "warmup_steps": zc_warm}
 
+    # ---- file-backed store leg (opt-in: writes the state to disk) ---------------
+    store = None
+    if args.store_dir:
+        store = run_store_leg(args, L, ptrs, buf0, buf1, hp_kw, device, world, rank)
+
     # ---- CPU baseline: the oracle on the host cores, bounded sample ------------
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -568,9 +577,11 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": "params/s", "h2d_bytes_per_step": h2d_b,
                     "d2h_bytes_per_step": d2h_b, "steps": e_steps, "call": "lst_stream_step",
                     "gpu_launches": e_steps * chunks},
+            "options": options,
             "stream": stream_info,
             "zero_copy": zero_copy,
             "stream_devgrad": stream_devgrad,
+            **({"store": store} if store is not None else {}),
             "cpu_baseline": cpu,
             "clocks": clk,
             "gpu_launches": args.steps,
@@ -580,6 +591,133 @@ def run_ours(args):
     if dist.is_available() and dist.is_initialized():
         dist.destroy_process_group()
     return 0
+
+
+def time_options_leg(args, L, dptrs, hp_kw, stream, device, world, t, flush, flush_rd, peak):
+    """Device-resident lst_adamw_step_ex, timed like the main leg (CUDA events
+    around each launch on the launching stream, L2 flushed before each when the
+    state is under twice the L2): per-block step counters t + (block mod 4) and
+    grad_sq for every block, so the extended kernel runs with its reduction."""
+    import torch
+    from optimizer_update_gb300 import lst
+    n = L.n_layers
+    gsq = torch.zeros(n, dtype=torch.float64, device=device)
+    ws = torch.empty(lst.lst_workspace_bytes(), dtype=torch.uint8, device=device)
+    opts = lst.step_options(block_steps=[t] * n, grad_sq=gsq.data_ptr(), workspace=ws.data_ptr())
+    steps_arr = opts._keep[0]
+    ptr_arr = lst._ptr_array(dptrs)
+    hp = lst.adamw_hparams(step=t, **hp_kw)
+    call = lst.lib().lst_adamw_step_ex
+    k_steps = max(3, args.steps // 2)
+
+    def launch(tt):
+        for i in range(n):
+            steps_arr[i] = tt + (i % 4)
+        hp.step = tt
+        st = call(L.handle, ptr_arr, ctypes.byref(hp), ctypes.byref(opts), stream.cuda_stream)
+        if st != lst.LST_OK:
+            raise lst.LstError(st, lst.lst_last_error())
+
+    for _ in range(3):
+        launch(t)
+        t += 1
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(k_steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(k_steps)]
+    torch.cuda.synchronize(device)
+    barrier(device)
+    for k in range(k_steps):
+        if flush is not None:
+            with torch.cuda.stream(stream):
+                flush.fill_(k & 0xFF)
+                flush_rd.sum()
+        starts[k].record(stream)
+        launch(t)
+        t += 1
+        ends[k].record(stream)
+    torch.cuda.synchronize(device)
+    per = [starts[k].elapsed_time(ends[k]) / 1e3 for k in range(k_steps)]
+    t_max = max_over_ranks(sum(per), device)
+    avg = sum(per) / k_steps
+    achieved = ALG_BYTES[L.fmt] * L.n_params / avg / 1e9
+    finite = bool(torch.isfinite(gsq).all().item()) and bool((gsq > 0).all().item())
+    return {"value": world * L.n_params * k_steps / t_max, "unit": "params/s", "call": "lst_adamw_step_ex",
+            "per_block_steps": True, "grad_sq": True, "achieved_gbs": achieved, "frac_of_hbm_peak": achieved / peak,
+            "avg_launch_ms": 1e3 * avg, "median_launch_ms": 1e3 * statistics.median(per), "steps": k_steps,
+            "grad_sq_all_positive_finite": finite}
+
+
+def disk_bandwidth(directory: str, nbytes: int, req: int = 64 << 20):
+    """Sequential direct-I/O write (then fsync) and read bandwidth of the file
+    system under `directory`, GB/s, over one `nbytes` file in `req` requests
+    (the access the block store makes); buffered I/O where O_DIRECT is refused."""
+    import mmap
+    path = os.path.join(directory, "disk_probe.bin")
+    buf = mmap.mmap(-1, req)
+    buf.write(bytes(range(256)) * (req // 256))
+    direct = getattr(os, "O_DIRECT", 0)
+    try:
+        fd = os.open(path, os.O_WRONLY | os.O_CREAT | os.O_TRUNC | direct, 0o644)
+    except OSError:
+        direct = 0
+        fd = os.open(path, os.O_WRONLY | os.O_CREAT | os.O_TRUNC, 0o644)
+    nbytes -= nbytes % req
+    t0 = time.perf_counter()
+    for off in range(0, nbytes, req):
+        os.pwrite(fd, buf, off)
+    os.fsync(fd)
+    tw = time.perf_counter() - t0
+    os.close(fd)
+    fd = os.open(path, os.O_RDONLY | direct)
+    t0 = time.perf_counter()
+    for off in range(0, nbytes, req):
+        os.preadv(fd, [buf], off)
+    tr = time.perf_counter() - t0
+    os.close(fd)
+    os.remove(path)
+    return nbytes / tw / 1e9, nbytes / tr / 1e9, bool(direct)
+
+
+def run_store_leg(args, L, ptrs, buf0, buf1, hp_kw, device, world, rank):
+    """lst_store_step over this workload's blocks in files under a fresh
+    directory inside --store-dir: the disk's own bandwidth measured first in
+    the same place, then one untimed and --store-steps timed store steps (each
+    reads every block file, runs the streamed step and commits every block
+    through a shadow file). Everything it writes is removed afterwards."""
+    import shutil
+    import tempfile
+    from optimizer_update_gb300 import lst
+    state = sum(L.block_bytes(i) for i in range(L.n_layers))
+    os.makedirs(args.store_dir, exist_ok=True)
+    free = shutil.disk_usage(args.store_dir).free
+    probe_bytes = min(4 << 30, max(256 << 20, state))
+    if free < 2 * state + probe_bytes + (1 << 30):
+        return {"skipped": f"{free} bytes free under the store directory, {2 * state + probe_bytes} needed"}
+    top = tempfile.mkdtemp(prefix=f"lst_store_r{rank}_", dir=args.store_dir)
+    staging = []
+    S = None
+    try:
+        w_gbs, r_gbs, direct = disk_bandwidth(top, probe_bytes)
+        S = lst.lst_store_create(L.handle, os.path.join(top, "blocks"), ptrs, 0)
+        staging = [lst.lst_host_alloc(L.max_block_bytes) for _ in range(3)]
+        lst.lst_store_step(S, staging, buf0.data_ptr(), buf1.data_ptr(), lst.adamw_hparams(step=1, **hp_kw), 600_000)
+        k = max(1, args.store_steps)
+        barrier(device)
+        t0 = time.perf_counter()
+        for t in range(2, 2 + k):
+            lst.lst_store_step(S, staging, buf0.data_ptr(), buf1.data_ptr(), lst.adamw_hparams(step=t, **hp_kw), 600_000)
+        dt = max_over_ranks(time.perf_counter() - t0, device) / k
+    finally:
+        if S is not None:
+            lst.lst_store_close(S)
+        for p in staging:
+            lst.lst_host_free(p)
+        shutil.rmtree(top, ignore_errors=True)
+    serial = state / (w_gbs * 1e9) + state / (r_gbs * 1e9)
+    return {"value": world * L.n_params / dt, "unit": "params/s", "call": "lst_store_step", "step_s": dt,
+            "file_read_bytes_per_step": state, "file_write_bytes_per_step": state,
+            "disk_write_gbs": w_gbs, "disk_read_gbs": r_gbs, "direct_io": direct,
+            "disk_serial_s": serial, "frac_of_disk_serial": serial / dt,
+            "frac_of_disk_write": state / (w_gbs * 1e9) / dt, "steps": k, "warmup_steps": 1}
 
 
 def main(argv=None):
@@ -594,6 +732,10 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--store-dir", default=None,
+                    help="also time lst_store_step with the blocks in files under this directory (writes twice "
+                         "the state to disk, removed afterwards)")
+    ap.add_argument("--store-steps", type=int, default=2)
     ap.add_argument("--max-blocks", type=int, default=0,
                     help="keep only the first N blocks of the workload (a smaller case)")
     args = ap.parse_args(argv)

@@ -203,19 +203,21 @@ typedef struct lst_step_options {
   /* DEVICE array [n_layers] of doubles, or NULL. When given, every block that
      is not skipped receives sum(g^2) over its elements (its squared gradient
      L2 norm), computed in the same pass as the update: per group of 8
-     elements in fp32, accumulated in fp64 in a fixed order (deterministic for
-     a given device). Entries of skipped blocks are left untouched. Written
-     asynchronously on the call's stream. */
+     elements in fp32, accumulated in an fp32 pair that recovers each
+     addition's rounding error exactly, then in fp64, in a fixed order
+     (deterministic for a given device). Entries of skipped blocks are left
+     untouched. Written asynchronously on the call's stream (by a second,
+     small launch after the update). */
   double* grad_sq;
   /* DEVICE scratch of lst_workspace_bytes() bytes, 256-byte aligned; required
      when grad_sq is given. Calls that share a workspace must not overlap on
-     the GPU. The library sets what must start at zero before each launch. */
+     the GPU. Its contents on entry do not matter. */
   void* workspace;
 } lst_step_options;
 
 /* Bytes of device workspace the sum-of-squares reduction needs (a constant:
    one fp64 partial per CTA, up to 1024 CTAs, and per block of one launch, up
-   to 128 blocks, plus a 256-byte header). */
+   to 128 blocks, after a reserved 256-byte header). */
 LST_API int64_t lst_workspace_bytes(void);
 
 /* lst_adamw_step with per-block options (opts may be NULL). Results of a

@@ -104,8 +104,8 @@ struct RunEx {
   int32_t accumulate;  // 1: add to the slot, 0: overwrite it
 };
 
-// Workspace of the sum-of-squares reduction: a counter, then one fp64
-// partial per (run, CTA) of a launch.
+// Workspace of the sum-of-squares reduction: a reserved 256-byte header, then
+// one fp64 partial per (run, CTA) of a launch.
 constexpr int kMaxGridEx = 1024;
 constexpr int64_t kWorkspaceHeader = 256;
 constexpr int64_t kWorkspaceBytes = kWorkspaceHeader + int64_t(8) * kMaxGridEx * kMaxRunsPerLaunch;

@@ -7,19 +7,23 @@
 
 namespace lst {
 
-// ---- the extended kernel: per-block step counters and per-block sum of g^2 ----
+// ---- the extended kernels: per-block step counters and per-block sum of g^2 ----
 //
 // Progressive layer locking ("Training 70B Models on Consumer Hardware",
 // section "Progressive Layer Locking") freezes a layer once its gradient
 // magnitude falls below a threshold; per-layer step counters keep Adam's bias
 // correction exact for the layers that keep training (same page, note under
-// "The Math"). This variant takes the bias corrections per run, and with
-// GSQ=true also returns sum(g^2) over every run as a by-product of the same
+// "The Math"). These variants take the bias corrections per run, and with
+// GSQ=true also return sum(g^2) over every run as a by-product of the same
 // pass: per task each lane adds its 8 squares in fp32 (exact products for bf16
-// g), accumulates tasks in fp64, the warp and the CTA reduce in a fixed order,
-// each CTA writes one partial per run to the workspace, and the last CTA to
-// finish adds the partials in CTA order. The result is deterministic for a
-// given grid.
+// g) and accumulates tasks in an fp32 pair with exact error recovery (below);
+// a warp reduces its lanes in fp64 in a fixed shuffle order, a CTA adds its
+// warps' sums per run in warp order and writes one partial per run to the
+// workspace, and a second small launch adds each run's partials in a fixed
+// order. The result is deterministic for a given grid.
+// Large launches walk run by run with the main kernel's prefetch schedule;
+// small ones (many short runs, e.g. LoRA adapters) walk their global tasks
+// across runs with a cursor, as the main small-launch kernel.
 
 struct RunTableEx {
   int32_t n;
@@ -60,12 +64,84 @@ __device__ __forceinline__ float sum_sq8(const float4& a, const float4& b) {
   return __fadd_rn(x, y);
 }
 
+// The running sum of a lane's task sums is kept as an unevaluated pair of
+// fp32 values hi + lo: each addition's rounding error is recovered exactly
+// (Knuth's TwoSum) and collected in lo, so the pair carries about twice
+// fp32's precision using fp32 adds only (this GPU has little fp64
+// throughput). It becomes one fp64 value when the lane leaves a run; a
+// non-finite hi is kept as it is (TwoSum would turn +inf into NaN).
+struct SumPair {
+  float hi, lo;
+};
+
+__device__ __forceinline__ void sum_pair_add(SumPair& p, float x) {
+  const float s = __fadd_rn(p.hi, x);
+  const float xb = __fsub_rn(s, p.hi);
+  const float hb = __fsub_rn(s, xb);
+  const float e = __fadd_rn(__fsub_rn(p.hi, hb), __fsub_rn(x, xb));
+  p.hi = s;
+  p.lo = __fadd_rn(p.lo, e);
+}
+
+__device__ __forceinline__ double sum_pair_value(const SumPair& p) {
+  return isfinite(p.hi) ? (double)p.hi + (double)p.lo : (double)p.hi;
+}
+
+// Sum over the warp's lanes in a fixed butterfly order (every lane gets it).
+__device__ __forceinline__ double warp_sum_f64(double x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Second launch of a step with sums: one CTA per run adds that run's partials
+// (one per CTA of the update launch, at most 4 per thread) and its threads'
+// sums in a fixed order. A separate launch needs no ticket counter, fence or
+// workspace initialisation, and reads every partial in one round.
+struct GradSqTable {
+  int32_t n;                  // runs of the update launch
+  int32_t partials_per_run;   // CTAs of the update launch
+  int32_t out_index[kMaxRunsPerLaunch];
+  int32_t accumulate[kMaxRunsPerLaunch];
+};
+static_assert(kMaxGridEx <= 4 * kThreads, "at most 4 partials per thread");
+
+__global__ void __launch_bounds__(kThreads) lst_grad_sq_reduce_kernel(const __grid_constant__ GradSqTable t,
+                                                                     const double* partials, double* grad_sq) {
+  __shared__ double warp_total[kThreads / 32];
+  const int r = blockIdx.x;
+  const int out = t.out_index[r];
+  if (out < 0) return;  // the whole CTA
+  const double* p = partials + (size_t)r * t.partials_per_run;
+  double a[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int c = threadIdx.x + k * kThreads;
+    a[k] = c < t.partials_per_run ? p[c] : 0.0;
+  }
+  const double x = warp_sum_f64((a[0] + a[1]) + (a[2] + a[3]));
+  if ((threadIdx.x & 31) == 0) warp_total[threadIdx.x >> 5] = x;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double sum = 0.0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) sum += warp_total[w];
+    grad_sq[out] = t.accumulate[r] ? grad_sq[out] + sum : sum;
+  }
+}
+
+// Large launches: warps issue the next task's loads before computing the
+// current one (register double-buffering), as the main kernel's prefetch
+// schedule. Register budgets, measured on GB300 with the sum of squares on
+// (fraction of the measured copy bandwidth, 1.1 G elements): the 12 B layout
+// is held to 3 resident CTAs of 256 threads per SM (0.957, against 0.832
+// uncapped and 0.888 with one task at a time); the 16 B layouts ask for no
+// minimum (0: 94 registers, 0.963; a minimum of one CTA per SM let the
+// compiler take 112 and measured 0.922).
 template <int FMT, bool GSQ>
-__global__ void __launch_bounds__(kThreads) lst_update_ex_kernel(const __grid_constant__ RunTableEx tab,
-                                                                 const Scalars s0, double* partials,
-                                                                 unsigned int* counter, double* grad_sq) {
+__global__ void __launch_bounds__(kThreads, (FMT == F_L12 ? 3 : 0))
+    lst_update_ex_kernel(const __grid_constant__ RunTableEx tab, const Scalars s0, double* partials) {
   __shared__ double warp_sum[kThreads / 32];
-  __shared__ int is_last;
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   const long long n_warps = (long long)gridDim.x * (kThreads / 32);
@@ -75,22 +151,35 @@ __global__ void __launch_bounds__(kThreads) lst_update_ex_kernel(const __grid_co
     Scalars s = s0;
     s.bias_correction1 = R.bias_correction1;
     s.bias_correction2 = R.bias_correction2;
-    double acc = 0.0;
+    SumPair acc{0.0f, 0.0f};
     long long j = (warp - R.first_task) % n_warps;
     if (j < 0) j += n_warps;
-    for (; j < R.tasks; j += n_warps) {
-      const long long e = j * 256 + lane * 4;
+    if (j < R.tasks) {
+      long long e = j * 256 + lane * 4;
       Quad<FMT, false> a, b;
       load_quad_ex<FMT>(R, e, a);
       load_quad_ex<FMT>(R, e + 128, b);
-      if (GSQ) acc += (double)sum_sq8(a.g, b.g);
-      store_quad_ex<FMT>(R, e, a, s);
-      store_quad_ex<FMT>(R, e + 128, b, s);
+      for (;;) {
+        const long long jn = j + n_warps;
+        const long long en = jn * 256 + lane * 4;
+        Quad<FMT, false> na, nb;
+        if (jn < R.tasks) {
+          load_quad_ex<FMT>(R, en, na);
+          load_quad_ex<FMT>(R, en + 128, nb);
+        }
+        if (GSQ) sum_pair_add(acc, sum_sq8(a.g, b.g));
+        store_quad_ex<FMT>(R, e, a, s);
+        store_quad_ex<FMT>(R, e + 128, b, s);
+        if (jn >= R.tasks) break;
+        a = na;
+        b = nb;
+        e = en;
+        j = jn;
+      }
     }
     if (GSQ) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) warp_sum[wid] = acc;
+      const double lane_sum = warp_sum_f64(sum_pair_value(acc));
+      if (lane == 0) warp_sum[wid] = lane_sum;
       __syncthreads();
       if (threadIdx.x == 0) {
         double c = 0.0;
@@ -101,21 +190,67 @@ __global__ void __launch_bounds__(kThreads) lst_update_ex_kernel(const __grid_co
       __syncthreads();
     }
   }
+}
+
+// Small launches: warp w takes global tasks w, w + n_warps, ... across run
+// boundaries (a register cursor moves forward through the run table), one
+// task at a time at 4 CTAs of 256 threads per SM. A warp meets each run in
+// one unbroken stretch of its tasks, so its sum for that run is final when
+// the cursor leaves the run: the warp stores it in shared memory (one slot
+// per warp and run), and at the end the CTA adds its warps' slots per run in
+// warp order.
+template <int FMT, bool GSQ>
+__global__ void __launch_bounds__(kThreads, 4)
+    lst_update_ex_small_kernel(const __grid_constant__ RunTableEx tab, const Scalars s0, double* partials,
+                               const long long total_tasks) {
+  __shared__ double run_sum[GSQ ? kThreads / 32 : 1][GSQ ? kMaxRunsPerLaunch : 1];
+  const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
   if (GSQ) {
-    __threadfence();
+    for (int i = threadIdx.x; i < (kThreads / 32) * kMaxRunsPerLaunch; i += kThreads) (&run_sum[0][0])[i] = 0.0;
     __syncthreads();
-    if (threadIdx.x == 0) is_last = (atomicAdd(counter, 1u) == gridDim.x - 1) ? 1 : 0;
-    __syncthreads();
-    if (is_last) {
-      __threadfence();
-      for (int r = threadIdx.x; r < tab.n; r += kThreads) {
-        const RunTableEx::Entry& R = tab.r[r];
-        if (R.out_index < 0) continue;
-        double sum = 0.0;
-        for (unsigned c = 0; c < gridDim.x; ++c) sum += __ldcg(&partials[(size_t)r * gridDim.x + c]);
-        grad_sq[R.out_index] = R.accumulate ? grad_sq[R.out_index] + sum : sum;
+  }
+  const long long n_warps = (long long)gridDim.x * (kThreads / 32);
+  long long g = (long long)blockIdx.x * (kThreads / 32) + wid;
+  int r = -1;
+  long long first = 0, end = 0;
+  Scalars s = s0;
+  SumPair acc{0.0f, 0.0f};
+  for (; g < total_tasks; g += n_warps) {
+    if (g >= end) {  // warp-uniform: g is the same in every lane
+      if (GSQ && r >= 0) {
+        const double warp_total = warp_sum_f64(sum_pair_value(acc));
+        if (lane == 0) run_sum[wid][r] = warp_total;
+        acc = SumPair{0.0f, 0.0f};
       }
-      if (threadIdx.x == 0) *counter = 0u;
+      do {
+        ++r;
+        first = tab.r[r].first_task;
+        end = first + tab.r[r].tasks;
+      } while (g >= end);
+      s.bias_correction1 = tab.r[r].bias_correction1;
+      s.bias_correction2 = tab.r[r].bias_correction2;
+    }
+    const RunTableEx::Entry& R = tab.r[r];
+    const long long e = (g - first) * 256 + lane * 4;
+    Quad<FMT, false> a, b;
+    load_quad_ex<FMT>(R, e, a);
+    load_quad_ex<FMT>(R, e + 128, b);
+    if (GSQ) sum_pair_add(acc, sum_sq8(a.g, b.g));
+    store_quad_ex<FMT>(R, e, a, s);
+    store_quad_ex<FMT>(R, e + 128, b, s);
+  }
+  if (GSQ) {
+    if (r >= 0) {
+      const double warp_total = warp_sum_f64(sum_pair_value(acc));
+      if (lane == 0) run_sum[wid][r] = warp_total;
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < tab.n; q += kThreads) {
+      double c = 0.0;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) c += run_sum[w][q];
+      partials[(size_t)q * gridDim.x + blockIdx.x] = c;
     }
   }
 }
@@ -123,13 +258,18 @@ __global__ void __launch_bounds__(kThreads) lst_update_ex_kernel(const __grid_co
 // Resident CTAs per SM for each instantiation, and SM count, per device.
 struct DeviceInfoEx {
   int sms = 0;
-  int ctas_per_sm[6] = {0, 0, 0, 0, 0, 0};
+  int ctas_per_sm[12] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 };
 constexpr int kMaxDevicesEx = 64;
 static DeviceInfoEx g_dev_ex[kMaxDevicesEx];
 static std::mutex g_dev_ex_mu;
 
-typedef void (*KernelExFn)(const RunTableEx, const Scalars, double*, unsigned int*, double*);
+// Below this many algorithmic bytes a launch uses the small-launch kernel (as
+// the main path: about twice the L2).
+constexpr long long kSmallLaunchBytesEx = 256ll << 20;
+
+typedef void (*KernelExFn)(const RunTableEx, const Scalars, double*);
+typedef void (*KernelExSmallFn)(const RunTableEx, const Scalars, double*, const long long);
 
 static KernelExFn kernel_ex_for(lst_format fmt, bool gsq) {
   switch (fmt) {
@@ -139,12 +279,22 @@ static KernelExFn kernel_ex_for(lst_format fmt, bool gsq) {
   }
 }
 
-static cudaError_t resident_ctas_ex(lst_format fmt, bool gsq, int* total) {
+static KernelExSmallFn kernel_ex_small_for(lst_format fmt, bool gsq) {
+  switch (fmt) {
+    case LST_L12_BF16:
+      return gsq ? lst_update_ex_small_kernel<F_L12, true> : lst_update_ex_small_kernel<F_L12, false>;
+    case LST_L16_MIXED:
+      return gsq ? lst_update_ex_small_kernel<F_L16M, true> : lst_update_ex_small_kernel<F_L16M, false>;
+    default: return gsq ? lst_update_ex_small_kernel<F_L16F, true> : lst_update_ex_small_kernel<F_L16F, false>;
+  }
+}
+
+static cudaError_t resident_ctas_ex(lst_format fmt, bool gsq, bool small, int* total) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevicesEx) return cudaErrorInvalidDevice;
-  const int slot = (int)fmt * 2 + (gsq ? 1 : 0);
+  const int slot = (int)fmt * 4 + (gsq ? 2 : 0) + (small ? 1 : 0);
   std::lock_guard<std::mutex> g(g_dev_ex_mu);
   DeviceInfoEx& d = g_dev_ex[dev];
   if (d.sms == 0) {
@@ -153,11 +303,15 @@ static cudaError_t resident_ctas_ex(lst_format fmt, bool gsq, int* total) {
   }
   if (d.ctas_per_sm[slot] == 0) {
     int n = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_ex_for(fmt, gsq), kThreads, 0);
+    err = small ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_ex_small_for(fmt, gsq), kThreads, 0)
+                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_ex_for(fmt, gsq), kThreads, 0);
     if (err != cudaSuccess) return err;
     d.ctas_per_sm[slot] = n > 0 ? n : 1;
   }
-  *total = d.sms * d.ctas_per_sm[slot];
+  // large launches: twice the resident CTAs, as the main kernels; small ones:
+  // one wave (fewer partial sums to add). At most kMaxGridEx: the workspace
+  // holds one partial sum per CTA and run.
+  *total = (small ? 1 : 2) * d.sms * d.ctas_per_sm[slot];
   if (*total > kMaxGridEx) *total = kMaxGridEx;
   return cudaSuccess;
 }
@@ -165,11 +319,7 @@ static cudaError_t resident_ctas_ex(lst_format fmt, bool gsq, int* total) {
 cudaError_t launch_update_ex(lst_format fmt, const RunEx* runs, int n_runs, const Scalars& s, void* workspace,
                              double* grad_sq, cudaStream_t stream) {
   const bool gsq = grad_sq != nullptr;
-  int max_ctas = 0;
-  cudaError_t err = resident_ctas_ex(fmt, gsq, &max_ctas);
-  if (err != cudaSuccess) return err;
-  KernelExFn fn = kernel_ex_for(fmt, gsq);
-  unsigned int* counter = gsq ? static_cast<unsigned int*>(workspace) : nullptr;
+  const FormatInfo& fi = format_info(fmt);
   double* partials = gsq ? reinterpret_cast<double*>(static_cast<char*>(workspace) + kWorkspaceHeader) : nullptr;
   int i = 0;
   while (i < n_runs) {
@@ -195,16 +345,33 @@ cudaError_t launch_update_ex(lst_format fmt, const RunEx* runs, int n_runs, cons
       tasks += e.tasks;
     }
     if (tab.n == 0) continue;
+    // algorithmic bytes of the launch: reads and writes of every element
+    const long long bytes = tasks * kWarpSpan * (long long)(fi.bytes_per_param + (fmt == LST_L12_BF16 ? 10 : 12));
+    const bool small = bytes < kSmallLaunchBytesEx;
+    int max_ctas = 0;
+    cudaError_t err = resident_ctas_ex(fmt, gsq, small, &max_ctas);
+    if (err != cudaSuccess) return err;
     long long grid = (tasks + kThreads / 32 - 1) / (kThreads / 32);
     if (grid < 1) grid = 1;
     if (grid > max_ctas) grid = max_ctas;
-    if (gsq) {
-      err = cudaMemsetAsync(counter, 0, sizeof(unsigned int), stream);
-      if (err != cudaSuccess) return err;
-    }
-    fn<<<(unsigned)grid, kThreads, 0, stream>>>(tab, s, partials, counter, grad_sq);
+    if (small)
+      kernel_ex_small_for(fmt, gsq)<<<(unsigned)grid, kThreads, 0, stream>>>(tab, s, partials, tasks);
+    else
+      kernel_ex_for(fmt, gsq)<<<(unsigned)grid, kThreads, 0, stream>>>(tab, s, partials);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    if (gsq) {
+      GradSqTable t;
+      t.n = tab.n;
+      t.partials_per_run = (int32_t)grid;
+      for (int k = 0; k < tab.n; ++k) {
+        t.out_index[k] = tab.r[k].out_index;
+        t.accumulate[k] = tab.r[k].accumulate;
+      }
+      lst_grad_sq_reduce_kernel<<<(unsigned)tab.n, kThreads, 0, stream>>>(t, partials, grad_sq);
+      err = cudaGetLastError();
+      if (err != cudaSuccess) return err;
+    }
   }
   return cudaSuccess;
 }

@@ -130,6 +130,44 @@ def test_grad_sq_lora_full_size():
 
 
 @pytest.mark.parametrize("fmt,workload", FMTS)
+def test_small_launches_many_ragged_blocks(fmt, workload):
+    """130 small blocks of ragged sizes (two launches of the cross-run
+    small-launch kernel): per-block steps, every 11th block locked, sum of g^2
+    for the rest; each block against the oracle, and the sums bit-identical on
+    a second call."""
+    specs = [(f"t{i}", ((i * 7919) % 6000 + 1,), i) for i in range(130)]
+    specs += [(f"u{i}", (3, (i * 31) % 700 + 1), i) for i in range(0, 130, 3)]
+    L = Layout(specs, fmt)
+    hosts = [np.empty(L.block_bytes(i), np.uint8) for i in range(L.n_layers)]
+    for i in range(L.n_layers):
+        fill_host_block(L, i, hosts[i], workload, 10)
+    steps = [1 + (i * 13) % 50 for i in range(L.n_layers)]
+    skip = [1 if i % 11 == 4 else 0 for i in range(L.n_layers)]
+    ws = _ws()
+    sums = []
+    for rep in range(2):
+        dev = [torch.from_numpy(h).cuda() for h in hosts]
+        gsq = torch.full((L.n_layers,), -1.0, dtype=torch.float64, device="cuda")
+        opts = lst.step_options(block_steps=steps, skip=skip, grad_sq=gsq.data_ptr(), workspace=ws.data_ptr())
+        lst.lst_adamw_step_ex(L.handle, [d.data_ptr() for d in dev], hparams_for(workload, 3)[0], opts,
+                              torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        sums.append(gsq.cpu().numpy())
+    g = sums[0]
+    assert np.array_equal(sums[0].view(np.uint64), sums[1].view(np.uint64))
+    for i in range(L.n_layers):
+        got = dev[i].cpu().numpy()
+        if skip[i]:
+            assert np.array_equal(got, hosts[i]) and g[i] == -1.0
+            continue
+        ref = hosts[i].copy()
+        oracle_step(L, ref, i, hparams_for(workload, steps[i])[1], threads=1)
+        compare(fmt, L.numpy_views(i, got), L.numpy_views(i, ref))
+        exp_g = oracle.grad_sq(L.numpy_views(i, hosts[i])["G"])
+        assert abs(g[i] - exp_g) <= GSQ_REL * exp_g, (i, g[i], exp_g)
+
+
+@pytest.mark.parametrize("fmt,workload", FMTS)
 @pytest.mark.parametrize("chunk", [0, 1 << 20])
 def test_stream_step_ex(fmt, workload, chunk):
     L, hosts = _setup(fmt, workload)

@@ -133,3 +133,12 @@ def test_argument_checks(layout, tmp_path):
         lst.lst_store_step(S, [buf.ctypes.data + 64] * 3, 4096, 8192, lst.adamw_hparams(step=1), 1000)
     assert e.value.status == lst.LST_ERR_ALIGNMENT
     lst.lst_store_close(S)
+
+
+def test_bench_disk_probe_cleans_up(tmp_path):
+    """The bench's disk probe (the bandwidth the store leg is judged against)
+    reports positive rates and leaves nothing behind."""
+    import bench
+    w, r, direct = bench.disk_bandwidth(str(tmp_path), 8 << 20, req=1 << 20)
+    assert w > 0 and r > 0 and isinstance(direct, bool)
+    assert list(tmp_path.iterdir()) == []
