@@ -221,6 +221,18 @@ def build_layout(workload: str, max_blocks: int = 0):
     return Layout(specs, fmt)
 
 
+def anon_huge_page_bytes() -> int:
+    """Bytes of this process's anonymous memory backed by transparent huge
+    pages (Linux /proc/self/smaps_rollup), 0 where unavailable."""
+    try:
+        for line in open("/proc/self/smaps_rollup"):
+            if line.startswith("AnonHugePages:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
 def alloc_pinned_state(L, workload: str, seed: int):
     import ctypes
     import numpy as np
@@ -378,6 +390,7 @@ def run_ours(args):
     chunk = 1 << 24  # 16 Mi elements per sub-chunk (the library default)
     L.set_stream_chunk(chunk)
     ptrs, arrs = alloc_pinned_state(L, args.workload, seed)
+    huge_bytes = anon_huge_page_bytes()  # the pinned blocks' share of huge pages
 
     # ---- device-resident leg -------------------------------------------------
     dev = []
@@ -458,12 +471,11 @@ def run_ours(args):
     # ---- streamed leg (the public end-to-end call) ------------------------------
     h2d_b = sum(L.transfer(i)[1] for i in range(L.n_layers))
     d2h_b = sum(L.transfer(i)[3] for i in range(L.n_layers))
-    # The first steps over freshly pinned blocks can run several times slower
-    # than the steady state when the host's free memory is physically
-    # scattered (measured: one physical run per block on a fresh host, 94 ms
-    # from the first step; ~365 runs after another process churned tens of GB,
-    # 200-900 ms for the first steps, then settling). Untimed warm-up steps
-    # until two in a row agree within 5 % (at least 3, at most 12).
+    # Host-link throughput on a shared host varies from moment to moment
+    # (single pinned copies measured at 57-150 GB/s instead of 210 now and
+    # then, whole steps several times slower than the roofline in such
+    # periods). Untimed warm-up steps until two in a row agree within 5 % (at
+    # least 3, at most 12); the link is measured again after the streamed legs.
     def warm(call):
         nonlocal t
         prev, n_warm = None, 0
@@ -498,7 +510,8 @@ def run_ours(args):
                        achieved_h2d_gbs=h2d_b * e_steps / t_e2e / 1e9,
                        achieved_d2h_gbs=d2h_b * e_steps / t_e2e / 1e9,
                        roofline_ms=1e3 * roof_t, frac_of_link_roofline=roof_t / (t_e2e / e_steps),
-                       chunk_elems=chunk, warmup_steps=stream_warm)
+                       chunk_elems=chunk, warmup_steps=stream_warm,
+                       host_huge_page_bytes=huge_bytes, host_state_bytes=state_bytes)
 
     # ---- streamed leg with device-resident gradients: only the state crosses
     # the link inbound (the gradients stand for what a backward pass leaves on
@@ -543,6 +556,9 @@ def run_ours(args):
     ze.record(zstream)
     torch.cuda.synchronize(device)
     t_zc = max_over_ranks(zs.elapsed_time(ze) / 1e3, device)
+    link_after = link_bandwidth(torch, [a0, a1], buf0, buf1, nb)
+    stream_info["link_after"] = {k: link_after[k] for k in ("h2d_gbs", "d2h_gbs", "h2d_concurrent_gbs",
+                                                             "d2h_concurrent_gbs")}
     zero_copy = {"value": world * P * e_steps / t_zc, "unit": "params/s", "call": "lst_zero_copy_step",
                  "step_ms": 1e3 * t_zc / e_steps, "link_bytes_per_step": h2d_b + d2h_b,
                  "frac_of_link_roofline": roof_t / (t_zc / e_steps), "steps": e_steps, "warmup_steps": zc_warm}
