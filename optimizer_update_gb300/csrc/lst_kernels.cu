@@ -171,8 +171,9 @@ typedef void (*KernelFn)(const RunTable, const Scalars, const long long);
 // elements, median of 10 launches, fraction of the measured HBM copy
 // bandwidth, several boxes): L16M prefetch 0.979-0.987 (one task
 // 0.936-0.940); L16F two tasks 0.964-0.987 (one task 0.940); L12 prefetch at
-// 3 CTAs per SM 0.968-0.980 (one task 0.917-0.943; two tasks 0.81). A grid of
-// twice the resident CTAs measured equal or better for every format.
+// 3 CTAs per SM 0.968-0.980 (one task 0.917-0.943; two tasks 0.81), with
+// grids of two waves of resident CTAs (the number of waves per launch size is
+// set by waves_for below).
 static KernelFn kernel_for(lst_format fmt, bool sgd, bool small) {
   if (small) {
     switch (fmt) {
@@ -194,7 +195,26 @@ static KernelFn kernel_for(lst_format fmt, bool sgd, bool small) {
 // writes stay in L2 and its reads take a few microseconds, so the latency of
 // the fp32 division chains dominates; it uses lst_update_small_kernel.
 constexpr long long kSmallLaunchBytes = 256ll << 20;  // about twice the L2
-constexpr int kGridPerResident = 2;
+
+// Waves of resident CTAs per launch (grid = waves x resident CTAs; each CTA
+// walks its tasks, so the work per CTA is the same). A second wave starts
+// mid-launch with a fresh ramp (first loads in flight), which a launch of a
+// few hundred microseconds notices; over a long launch, extra waves let the
+// SMs that finish early take more CTAs. Measured on GB300 (fraction of the
+// copy bandwidth, 1, 2, 3, 4 waves): one 44 M-element 12 B layer (969 MB)
+// 0.946 / 0.933 / 0.933 / 0.921; 1.1 G elements 12 B 0.961 / 0.962 / 0.961 /
+// 0.960; 1.1 G elements 16 B mixed 0.964 / 0.970 / 0.973 / 0.973; and, 2
+// against 1 or 3 waves: a 44 M-element 16 B mixed layer (1.2 GB) 0.928-0.932
+// against 0.934-0.937 with one; 154 M elements 16 B mixed (4.3 GB) 0.965
+// against 0.962-0.964 with three; 1.1 G elements fp32 0.970-0.973 against
+// 0.976-0.978 with three.
+constexpr long long kOneWaveBytes = 2ll << 30;
+constexpr long long kThreeWaveBytes = 8ll << 30;
+static int waves_for(lst_format fmt, long long bytes) {
+  if (bytes < kOneWaveBytes) return 1;
+  if (fmt == LST_L12_BF16 || bytes < kThreeWaveBytes) return 2;
+  return 3;
+}
 
 // Resident CTAs per SM for each kernel instantiation, and SM count, per device.
 struct DeviceInfo {
@@ -205,7 +225,7 @@ constexpr int kMaxDevices = 64;
 static DeviceInfo g_dev[kMaxDevices];
 static std::mutex g_dev_mu;
 
-static cudaError_t resident_ctas(lst_format fmt, bool sgd, bool small, int* total) {
+static cudaError_t resident_ctas(lst_format fmt, bool sgd, bool small, int* total) {  // per wave
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -223,7 +243,7 @@ static cudaError_t resident_ctas(lst_format fmt, bool sgd, bool small, int* tota
     if (err != cudaSuccess) return err;
     d.ctas_per_sm[slot] = n > 0 ? n : 1;
   }
-  *total = d.sms * d.ctas_per_sm[slot] * (sgd ? 1 : kGridPerResident);
+  *total = d.sms * d.ctas_per_sm[slot];
   return cudaSuccess;
 }
 
@@ -253,9 +273,11 @@ cudaError_t launch_update(lst_format fmt, bool sgd, const Run* runs, int n_runs,
     // algorithmic bytes of the launch: reads and writes of every element
     const long long bytes = tasks * kWarpSpan * (long long)(fi.bytes_per_param + (fmt == LST_L12_BF16 ? 10 : 12));
     const bool small = bytes < kSmallLaunchBytes;
-    int max_ctas = 0;
-    cudaError_t err = resident_ctas(fmt, sgd, small, &max_ctas);
+    int per_wave = 0;
+    cudaError_t err = resident_ctas(fmt, sgd, small, &per_wave);
     if (err != cudaSuccess) return err;
+    // small launches: two waves of the 4-CTA-per-SM kernel; SGD: one wave
+    const long long max_ctas = (long long)per_wave * (small ? 2 : sgd ? 1 : waves_for(fmt, bytes));
     const long long warps_per_cta = kThreads / 32;
     long long grid = (tasks + warps_per_cta - 1) / warps_per_cta;
     if (grid > max_ctas) grid = max_ctas;
