@@ -104,6 +104,27 @@ struct RunEx {
   int32_t accumulate;  // 1: add to the slot, 0: overwrite it
 };
 
+// Waves of resident CTAs per launch of the large-launch update kernels (grid
+// = waves x resident CTAs; each CTA walks its tasks, so the work per CTA is
+// the same). A second wave starts
+// mid-launch with a fresh ramp (first loads in flight), which a launch of a
+// few hundred microseconds notices; over a long launch, extra waves let the
+// SMs that finish early take more CTAs. Measured on GB300 (fraction of the
+// copy bandwidth, 1, 2, 3, 4 waves): one 44 M-element 12 B layer (969 MB)
+// 0.946 / 0.933 / 0.933 / 0.921; 1.1 G elements 12 B 0.961 / 0.962 / 0.961 /
+// 0.960; 1.1 G elements 16 B mixed 0.964 / 0.970 / 0.973 / 0.973; and, 2
+// against 1 or 3 waves: a 44 M-element 16 B mixed layer (1.2 GB) 0.928-0.932
+// against 0.934-0.937 with one; 154 M elements 16 B mixed (4.3 GB) 0.965
+// against 0.962-0.964 with three; 1.1 G elements fp32 0.970-0.973 against
+// 0.976-0.978 with three.
+constexpr long long kOneWaveBytes = 2ll << 30;
+constexpr long long kThreeWaveBytes = 8ll << 30;
+inline int launch_waves(lst_format fmt, long long bytes) {
+  if (bytes < kOneWaveBytes) return 1;
+  if (fmt == LST_L12_BF16 || bytes < kThreeWaveBytes) return 2;
+  return 3;
+}
+
 // Workspace of the sum-of-squares reduction: a reserved 256-byte header, then
 // one fp64 partial per (run, CTA) of a launch.
 constexpr int kMaxGridEx = 1024;

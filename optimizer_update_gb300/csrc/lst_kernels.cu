@@ -196,25 +196,6 @@ static KernelFn kernel_for(lst_format fmt, bool sgd, bool small) {
 // the fp32 division chains dominates; it uses lst_update_small_kernel.
 constexpr long long kSmallLaunchBytes = 256ll << 20;  // about twice the L2
 
-// Waves of resident CTAs per launch (grid = waves x resident CTAs; each CTA
-// walks its tasks, so the work per CTA is the same). A second wave starts
-// mid-launch with a fresh ramp (first loads in flight), which a launch of a
-// few hundred microseconds notices; over a long launch, extra waves let the
-// SMs that finish early take more CTAs. Measured on GB300 (fraction of the
-// copy bandwidth, 1, 2, 3, 4 waves): one 44 M-element 12 B layer (969 MB)
-// 0.946 / 0.933 / 0.933 / 0.921; 1.1 G elements 12 B 0.961 / 0.962 / 0.961 /
-// 0.960; 1.1 G elements 16 B mixed 0.964 / 0.970 / 0.973 / 0.973; and, 2
-// against 1 or 3 waves: a 44 M-element 16 B mixed layer (1.2 GB) 0.928-0.932
-// against 0.934-0.937 with one; 154 M elements 16 B mixed (4.3 GB) 0.965
-// against 0.962-0.964 with three; 1.1 G elements fp32 0.970-0.973 against
-// 0.976-0.978 with three.
-constexpr long long kOneWaveBytes = 2ll << 30;
-constexpr long long kThreeWaveBytes = 8ll << 30;
-static int waves_for(lst_format fmt, long long bytes) {
-  if (bytes < kOneWaveBytes) return 1;
-  if (fmt == LST_L12_BF16 || bytes < kThreeWaveBytes) return 2;
-  return 3;
-}
 
 // Resident CTAs per SM for each kernel instantiation, and SM count, per device.
 struct DeviceInfo {
@@ -277,7 +258,7 @@ cudaError_t launch_update(lst_format fmt, bool sgd, const Run* runs, int n_runs,
     cudaError_t err = resident_ctas(fmt, sgd, small, &per_wave);
     if (err != cudaSuccess) return err;
     // small launches: two waves of the 4-CTA-per-SM kernel; SGD: one wave
-    const long long max_ctas = (long long)per_wave * (small ? 2 : sgd ? 1 : waves_for(fmt, bytes));
+    const long long max_ctas = (long long)per_wave * (small ? 2 : sgd ? 1 : launch_waves(fmt, bytes));
     const long long warps_per_cta = kThreads / 32;
     long long grid = (tasks + warps_per_cta - 1) / warps_per_cta;
     if (grid > max_ctas) grid = max_ctas;

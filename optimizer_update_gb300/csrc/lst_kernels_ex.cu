@@ -289,7 +289,7 @@ static KernelExSmallFn kernel_ex_small_for(lst_format fmt, bool gsq) {
   }
 }
 
-static cudaError_t resident_ctas_ex(lst_format fmt, bool gsq, bool small, int* total) {
+static cudaError_t resident_ctas_ex(lst_format fmt, bool gsq, bool small, int* total) {  // per wave
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -308,11 +308,7 @@ static cudaError_t resident_ctas_ex(lst_format fmt, bool gsq, bool small, int* t
     if (err != cudaSuccess) return err;
     d.ctas_per_sm[slot] = n > 0 ? n : 1;
   }
-  // large launches: twice the resident CTAs, as the main kernels; small ones:
-  // one wave (fewer partial sums to add). At most kMaxGridEx: the workspace
-  // holds one partial sum per CTA and run.
-  *total = (small ? 1 : 2) * d.sms * d.ctas_per_sm[slot];
-  if (*total > kMaxGridEx) *total = kMaxGridEx;
+  *total = d.sms * d.ctas_per_sm[slot];  // one wave
   return cudaSuccess;
 }
 
@@ -348,9 +344,14 @@ cudaError_t launch_update_ex(lst_format fmt, const RunEx* runs, int n_runs, cons
     // algorithmic bytes of the launch: reads and writes of every element
     const long long bytes = tasks * kWarpSpan * (long long)(fi.bytes_per_param + (fmt == LST_L12_BF16 ? 10 : 12));
     const bool small = bytes < kSmallLaunchBytesEx;
-    int max_ctas = 0;
-    cudaError_t err = resident_ctas_ex(fmt, gsq, small, &max_ctas);
+    int per_wave = 0;
+    cudaError_t err = resident_ctas_ex(fmt, gsq, small, &per_wave);
     if (err != cudaSuccess) return err;
+    // large launches: waves as the main kernel; small ones: one wave (fewer
+    // partial sums to add). At most kMaxGridEx: the workspace holds one
+    // partial sum per CTA and run.
+    long long max_ctas = (long long)per_wave * (small ? 1 : launch_waves(fmt, bytes));
+    if (max_ctas > kMaxGridEx) max_ctas = kMaxGridEx;
     long long grid = (tasks + kThreads / 32 - 1) / (kThreads / 32);
     if (grid < 1) grid = 1;
     if (grid > max_ctas) grid = max_ctas;
