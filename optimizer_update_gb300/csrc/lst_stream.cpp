@@ -35,6 +35,7 @@ struct Engine {
   cudaEvent_t update_done[2] = {nullptr, nullptr};
   cudaEvent_t buffer_free[2] = {nullptr, nullptr};
   cudaEvent_t done = nullptr;
+  size_t max_pitch = 0;  // the device's largest pitch for 2D copies
 };
 
 static void release(Engine* e) {
@@ -64,6 +65,9 @@ void destroy_engine(Engine* e) {
 static cudaError_t create(Engine* e, int device) {
   e->device = device;
   cudaError_t err;
+  int pitch = 0;
+  if ((err = cudaDeviceGetAttribute(&pitch, cudaDevAttrMaxPitch, device)) != cudaSuccess) return err;
+  e->max_pitch = pitch > 0 ? (size_t)pitch : 0;
   const unsigned f = cudaStreamNonBlocking;
   if ((err = cudaStreamCreateWithFlags(&e->h2d, f)) != cudaSuccess) return err;
   if ((err = cudaStreamCreateWithFlags(&e->compute, f)) != cudaSuccess) return err;
@@ -103,6 +107,20 @@ struct CopyOp {
 static cudaError_t do_copy(void* p) {
   CopyOp* c = static_cast<CopyOp*>(p);
   return cudaMemcpyAsync(c->dst, c->src, c->bytes, c->dir, c->st);
+}
+// Rows of equal length at the same stride on both sides: the chunk ranges of
+// consecutive segments with the same element size (segments are contiguous,
+// each padded * element-size bytes long).
+struct Copy2DOp {
+  void* dst;
+  const void* src;
+  size_t pitch, width, rows;
+  cudaMemcpyKind dir;
+  cudaStream_t st;
+};
+static cudaError_t do_copy2d(void* p) {
+  Copy2DOp* c = static_cast<Copy2DOp*>(p);
+  return cudaMemcpy2DAsync(c->dst, c->pitch, c->src, c->pitch, c->width, c->rows, c->dir, c->st);
 }
 struct RecordOp {
   cudaEvent_t ev;
@@ -167,6 +185,43 @@ static std::vector<int64_t> chunk_cuts(int64_t padded, int64_t C, bool first_blo
   std::vector<int64_t> cuts(1, 0);
   for (int64_t c : sizes) cuts.push_back(cuts.back() + c);
   return cuts;
+}
+
+// Enqueues the copies of elements [e0, e1) of segments [k0, k1) of a block
+// between `from` and `to` (same layout on both sides). Consecutive segments
+// with the same element size go as one 2D copy (one row per segment, the
+// segment's byte length as the pitch), so a sub-chunk of the mixed layout is
+// two copies per direction instead of four: fewer, larger copy-engine
+// operations. Falls back to one copy per segment where the pitch exceeds the
+// device's limit.
+static cudaError_t enqueue_range(Enqueuer& enq, const Engine* E, const FormatInfo& fi, const Block& b, int k0, int k1,
+                                 int64_t e0, int64_t e1, char* to, const char* from, cudaMemcpyKind dir,
+                                 cudaStream_t st) {
+  int k = k0;
+  while (k < k1) {
+    const int64_t eb = fi.elem_bytes[k];
+    const size_t pitch = (size_t)(b.padded * eb);
+    int k2 = k + 1;
+    while (k2 < k1 && fi.elem_bytes[k2] == eb &&
+           b.seg_off[fi.field[k2]] == b.seg_off[fi.field[k2 - 1]] + (int64_t)pitch)
+      ++k2;
+    const int64_t off = b.seg_off[fi.field[k]] + e0 * eb;
+    const size_t width = (size_t)((e1 - e0) * eb);
+    if (k2 - k > 1 && pitch <= E->max_pitch) {
+      Copy2DOp c{to + off, from + off, pitch, width, (size_t)(k2 - k), dir, st};
+      cudaError_t err = enq(do_copy2d, &c);
+      if (err != cudaSuccess) return err;
+    } else {
+      for (int j = k; j < k2; ++j) {
+        const int64_t o = b.seg_off[fi.field[j]] + e0 * eb;
+        CopyOp c{to + o, from + o, width, dir, st};
+        cudaError_t err = enq(do_copy, &c);
+        if (err != cudaSuccess) return err;
+      }
+    }
+    k = k2;
+  }
+  return cudaSuccess;
 }
 
 static void drain(Engine* e) {
@@ -311,13 +366,8 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
         CopyOp c{buf + off, host + off, (size_t)(b.h2d_off + b.h2d_bytes - off), cudaMemcpyHostToDevice, E->h2d};
         if ((err = enq(do_copy, &c)) != cudaSuccess) { what = "copy in"; break; }
       } else {
-        for (int k = first_in; k < fi.n_inputs && !what; ++k) {
-          const int64_t off = b.seg_off[fi.field[k]] + e0 * fi.elem_bytes[k];
-          CopyOp c{buf + off, host + off, (size_t)((e1 - e0) * fi.elem_bytes[k]), cudaMemcpyHostToDevice,
-                   E->h2d};
-          if ((err = enq(do_copy, &c)) != cudaSuccess) what = "copy in";
-        }
-        if (what) break;
+        err = enqueue_range(enq, E, fi, b, first_in, fi.n_inputs, e0, e1, buf, host, cudaMemcpyHostToDevice, E->h2d);
+        if (err != cudaSuccess) { what = "copy in"; break; }
       }
       RecordOp r1{E->weights_ready[bi], E->h2d};
       if ((err = enq(do_record, &r1)) != cudaSuccess) { what = "record weights-ready"; break; }
@@ -342,13 +392,9 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
         CopyOp c{host + b.d2h_off, buf + b.d2h_off, (size_t)b.d2h_bytes, cudaMemcpyDeviceToHost, E->d2h};
         if ((err = enq(do_copy, &c)) != cudaSuccess) { what = "copy out"; break; }
       } else {
-        for (int k = fi.first_output; k < fi.n_segments && !what; ++k) {
-          const int64_t off = b.seg_off[fi.field[k]] + e0 * fi.elem_bytes[k];
-          CopyOp c{host + off, buf + off, (size_t)((e1 - e0) * fi.elem_bytes[k]), cudaMemcpyDeviceToHost,
-                   E->d2h};
-          if ((err = enq(do_copy, &c)) != cudaSuccess) what = "copy out";
-        }
-        if (what) break;
+        err = enqueue_range(enq, E, fi, b, fi.first_output, fi.n_segments, e0, e1, host, buf, cudaMemcpyDeviceToHost,
+                            E->d2h);
+        if (err != cudaSuccess) { what = "copy out"; break; }
       }
     }
     if (what) break;
