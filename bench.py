@@ -337,6 +337,25 @@ def config_for(L, workload, world, max_blocks=0):
             "hparams": HP_LORA if L.fmt == "L16F" else HP}
 
 
+def block_h2d_rates(torch, arrs, dev):
+    """Host-to-device rate of each pinned block, one whole-block copy each
+    (GB/s, CUDA events on one stream): on a host where some pinned
+    allocations are slow, this names them."""
+    s = torch.cuda.Stream()
+    out = []
+    for a in arrs:
+        n = a.size
+        h = torch.from_numpy(a)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            dev[:n].copy_(h, non_blocking=True)
+            e1.record(s)
+        e1.synchronize()
+        out.append(n / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    return out
+
+
 def link_bandwidth(torch, host_ptr_arrs, dev_a, dev_b, nbytes: int, reps: int = 5):
     """Pinned host <-> device copy bandwidth: H2D alone, D2H alone, both at once
     (each direction timed on its own stream with CUDA events)."""
@@ -491,6 +510,9 @@ def run_ours(args):
 
     stream_warm = warm(lambda tt: lst.lst_stream_step(L.handle, ptrs, buf0.data_ptr(), buf1.data_ptr(),
                                                       lst.adamw_hparams(step=tt, **hp_kw), 600_000))
+    # every block's own host-to-device rate, after the warm-up and right
+    # before the timed steps (a slow pinned allocation holds up the pipeline)
+    block_rates = block_h2d_rates(torch, arrs, buf0)
     e_steps = max(1, min(args.steps, args.e2e_steps))
     barrier(device)
     t0 = time.perf_counter()
@@ -511,7 +533,9 @@ def run_ours(args):
                        achieved_d2h_gbs=d2h_b * e_steps / t_e2e / 1e9,
                        roofline_ms=1e3 * roof_t, frac_of_link_roofline=roof_t / (t_e2e / e_steps),
                        chunk_elems=chunk, warmup_steps=stream_warm,
-                       host_huge_page_bytes=huge_bytes, host_state_bytes=state_bytes)
+                       host_huge_page_bytes=huge_bytes, host_state_bytes=state_bytes,
+                       block_h2d_gbs_min=min(block_rates), block_h2d_gbs_median=statistics.median(block_rates),
+                       slow_blocks=sum(1 for r in block_rates if r < 0.5 * link["h2d_gbs"]))
 
     # ---- streamed leg with device-resident gradients: only the state crosses
     # the link inbound (the gradients stand for what a backward pass leaves on
