@@ -58,6 +58,9 @@ WORKLOADS = {
 }
 # Algorithmic bytes per parameter of one device-resident step (reads + writes).
 ALG_BYTES = {"L12": 22, "L16M": 28, "L16F": 28}
+# ... and of one SGD step (G and W read, W written; the mixed layout reads the
+# fp32 master and writes it and the bf16 W; m and v are untouched)
+SGD_BYTES = {"L12": 6, "L16M": 12, "L16F": 12}
 # algorithmic bytes below which the launch path uses lst_update_small_kernel
 # (kSmallLaunchBytes in lst_kernels.cu: about twice the 129 MB L2)
 SMALL_LAUNCH_BYTES = 256 << 20
@@ -475,6 +478,7 @@ def run_ours(args):
     # block (staggered, as after progressive locking) and every block's
     # sum of g^2 returned by the same pass ---------------------------------------
     options = time_options_leg(args, L, dptrs, hp_kw, stream, device, world, t, flush, flush_rd, peak)
+    sgd = time_sgd_leg(args, L, dptrs, hp_kw, stream, device, world, flush, flush_rd, peak)
     del dev
     torch.cuda.empty_cache()
 
@@ -618,6 +622,7 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h_b, "steps": e_steps, "call": "lst_stream_step",
                     "gpu_launches": e_steps * chunks},
             "options": options,
+            "sgd": sgd,
             "stream": stream_info,
             "zero_copy": zero_copy,
             "stream_devgrad": stream_devgrad,
@@ -684,6 +689,44 @@ def time_options_leg(args, L, dptrs, hp_kw, stream, device, world, t, flush, flu
             "per_block_steps": True, "grad_sq": True, "achieved_gbs": achieved, "frac_of_hbm_peak": achieved / peak,
             "avg_launch_ms": 1e3 * avg, "median_launch_ms": 1e3 * statistics.median(per), "steps": k_steps,
             "grad_sq_all_positive_finite": finite}
+
+
+def time_sgd_leg(args, L, dptrs, hp_kw, stream, device, world, flush, flush_rd, peak):
+    """Device-resident lst_sgd_step (W += -lr*g), timed like the main leg."""
+    import torch
+    from optimizer_update_gb300 import lst
+    ptr_arr = lst._ptr_array(dptrs)
+    call = lst.lib().lst_sgd_step
+    lr = ctypes.c_float(hp_kw["lr"])
+    k_steps = max(3, args.steps // 2)
+
+    def launch():
+        st = call(L.handle, ptr_arr, lr, stream.cuda_stream)
+        if st != lst.LST_OK:
+            raise lst.LstError(st, lst.lst_last_error())
+
+    for _ in range(3):
+        launch()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(k_steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(k_steps)]
+    torch.cuda.synchronize(device)
+    barrier(device)
+    for k in range(k_steps):
+        if flush is not None:
+            with torch.cuda.stream(stream):
+                flush.fill_(k & 0xFF)
+                flush_rd.sum()
+        starts[k].record(stream)
+        launch()
+        ends[k].record(stream)
+    torch.cuda.synchronize(device)
+    per = [starts[k].elapsed_time(ends[k]) / 1e3 for k in range(k_steps)]
+    t_max = max_over_ranks(sum(per), device)
+    avg = sum(per) / k_steps
+    achieved = SGD_BYTES[L.fmt] * L.n_params / avg / 1e9
+    return {"value": world * L.n_params * k_steps / t_max, "unit": "params/s", "call": "lst_sgd_step",
+            "alg_bytes_per_param": SGD_BYTES[L.fmt], "achieved_gbs": achieved, "frac_of_hbm_peak": achieved / peak,
+            "avg_launch_ms": 1e3 * avg, "median_launch_ms": 1e3 * statistics.median(per), "steps": k_steps}
 
 
 def disk_bandwidth(directory: str, nbytes: int, req: int = 64 << 20):

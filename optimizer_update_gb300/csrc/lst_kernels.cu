@@ -182,13 +182,17 @@ static KernelFn kernel_for(lst_format fmt, bool sgd, bool small) {
       default: return sgd ? lst_update_small_kernel<F_L16F, true> : lst_update_small_kernel<F_L16F, false>;
     }
   }
+  // SGD (W += -lr*g: little arithmetic per byte), same measurement with the
+  // launch-size waves: 12 B one task 0.996-0.998 (prefetch 0.972-0.978, two
+  // tasks 0.915-0.922); 16 B mixed prefetch 0.958-0.961 (one task
+  // 0.953-0.954, two tasks 0.953-0.954; one task in one wave 0.939-0.940).
   switch (fmt) {
     case LST_L12_BF16:
       return sgd ? lst_update_kernel<F_L12, true, SCHED_ONE> : lst_update_kernel<F_L12, false, SCHED_PREFETCH>;
     case LST_L16_MIXED:
-      return sgd ? lst_update_kernel<F_L16M, true, SCHED_ONE> : lst_update_kernel<F_L16M, false, SCHED_PREFETCH>;
+      return sgd ? lst_update_kernel<F_L16M, true, SCHED_PREFETCH> : lst_update_kernel<F_L16M, false, SCHED_PREFETCH>;
     default:
-      return sgd ? lst_update_kernel<F_L16F, true, SCHED_ONE> : lst_update_kernel<F_L16F, false, SCHED_TWO>;
+      return sgd ? lst_update_kernel<F_L16F, true, SCHED_PREFETCH> : lst_update_kernel<F_L16F, false, SCHED_TWO>;
   }
 }
 // A launch moving less than this many algorithmic bytes is not HBM-bound: its
@@ -257,8 +261,8 @@ cudaError_t launch_update(lst_format fmt, bool sgd, const Run* runs, int n_runs,
     int per_wave = 0;
     cudaError_t err = resident_ctas(fmt, sgd, small, &per_wave);
     if (err != cudaSuccess) return err;
-    // small launches: two waves of the 4-CTA-per-SM kernel; SGD: one wave
-    const long long max_ctas = (long long)per_wave * (small ? 2 : sgd ? 1 : launch_waves(fmt, bytes));
+    // small launches: two waves of the 4-CTA-per-SM kernel
+    const long long max_ctas = (long long)per_wave * (small ? 2 : launch_waves(fmt, bytes));
     const long long warps_per_cta = kThreads / 32;
     long long grid = (tasks + warps_per_cta - 1) / warps_per_cta;
     if (grid > max_ctas) grid = max_ctas;
