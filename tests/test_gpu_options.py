@@ -17,7 +17,8 @@ import oracle
 from optimizer_update_gb300 import Layout, lst
 from synth import shapes
 
-from gpu_util import PinnedBlocks, compare, fill_host_block, hparams_for, oracle_step
+from gpu_util import (PinnedBlocks, compare, fill_host_block, gather_device, gathered_inputs, hparams_for,
+                      oracle_step, sample_indices)
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -165,6 +166,51 @@ def test_small_launches_many_ragged_blocks(fmt, workload):
         compare(fmt, L.numpy_views(i, got), L.numpy_views(i, ref))
         exp_g = oracle.grad_sq(L.numpy_views(i, hosts[i])["G"])
         assert abs(g[i] - exp_g) <= GSQ_REL * exp_g, (i, g[i], exp_g)
+
+
+@pytest.mark.slow
+def test_full_size_mixed_layout_sampled():
+    """The whole TinyLlama-1.1B mixed-layout state (17.6 GB) in one extended
+    launch, as the bench times it (three waves of CTAs): per-block steps
+    t + (block mod 4), block 5 locked, sums of g^2 for the rest. Sampled
+    elements of every block against the oracle at that block's own step, the
+    locked block bit-untouched, every sum against the oracle's."""
+    fmt, workload, t = "L16M", "tinyllama_full_l16m", 10
+    L = Layout(shapes.tinyllama_full(), fmt)
+    host = np.empty(L.max_block_bytes, np.uint8)
+    blocks, exp_g = [], []
+    for i in range(L.n_layers):
+        n = L.block_bytes(i)
+        fill_host_block(L, i, host[:n], workload, t)
+        exp_g.append(oracle.grad_sq(L.numpy_views(i, host[:n])["G"]))
+        b = torch.empty(n, dtype=torch.uint8, device="cuda")
+        b.copy_(torch.from_numpy(host[:n]))
+        blocks.append(b)
+    locked = 5
+    before = blocks[locked].clone()
+    steps = [t + i % 4 for i in range(L.n_layers)]
+    skip = [1 if i == locked else 0 for i in range(L.n_layers)]
+    gsq = torch.full((L.n_layers,), -1.0, dtype=torch.float64, device="cuda")
+    ws = _ws()
+    opts = lst.step_options(block_steps=steps, skip=skip, grad_sq=gsq.data_ptr(), workspace=ws.data_ptr())
+    lst.lst_adamw_step_ex(L.handle, [b.data_ptr() for b in blocks], hparams_for(workload, t)[0], opts,
+                          torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert torch.equal(blocks[locked], before)
+    g = gsq.cpu().numpy()
+    rng = np.random.default_rng(7)
+    checked = 0
+    for i in range(L.n_layers):
+        if i == locked:
+            assert g[i] == -1.0
+            continue
+        assert abs(g[i] - exp_g[i]) <= GSQ_REL * exp_g[i], (i, g[i], exp_g[i])
+        idx = sample_indices(L.padded(i), L.spans(i), rng, n_random=4096)
+        inp = gathered_inputs(L, i, workload, t, idx)
+        oracle.step(fmt, inp, hparams_for(workload, steps[i])[1])
+        compare(fmt, gather_device(L.torch_views(i, blocks[i]), idx), inp)
+        checked += idx.size
+    assert checked > 50_000
 
 
 @pytest.mark.parametrize("fmt,workload", FMTS)
