@@ -94,6 +94,19 @@ __device__ __forceinline__ double warp_sum_f64(double x) {
   return x;
 }
 
+// Programmatic dependent launch (PTX griddepcontrol): the update grid's CTAs
+// signal once their partial sums are written, so the reduce grid that follows
+// on the stream may be scheduled before the update grid has fully retired;
+// the reduce grid waits (in hardware) until the update grid has completed and
+// its memory is visible before it reads a partial. The wait ends when the
+// update grid ends, so nothing here can hang.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_for_prerequisite_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Second launch of a step with sums: one CTA per run adds that run's partials
 // (one per CTA of the update launch, at most 4 per thread) and its threads'
 // sums in a fixed order. A separate launch needs no ticket counter, fence or
@@ -109,6 +122,7 @@ static_assert(kMaxGridEx <= 4 * kThreads, "at most 4 partials per thread");
 __global__ void __launch_bounds__(kThreads) lst_grad_sq_reduce_kernel(const __grid_constant__ GradSqTable t,
                                                                      const double* partials, double* grad_sq) {
   __shared__ double warp_total[kThreads / 32];
+  wait_for_prerequisite_grid();
   const int r = blockIdx.x;
   const int out = t.out_index[r];
   if (out < 0) return;  // the whole CTA
@@ -190,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, (FMT == F_L12 ? 3 : 0))
       __syncthreads();
     }
   }
+  if (GSQ) allow_dependent_launch();
 }
 
 // Small launches: warp w takes global tasks w, w + n_warps, ... across run
@@ -252,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 4)
       for (int w = 0; w < kThreads / 32; ++w) c += run_sum[w][q];
       partials[(size_t)q * gridDim.x + blockIdx.x] = c;
     }
+    allow_dependent_launch();
   }
 }
 
@@ -369,8 +385,17 @@ cudaError_t launch_update_ex(lst_format fmt, const RunEx* runs, int n_runs, cons
         t.out_index[k] = tab.r[k].out_index;
         t.accumulate[k] = tab.r[k].accumulate;
       }
-      lst_grad_sq_reduce_kernel<<<(unsigned)tab.n, kThreads, 0, stream>>>(t, partials, grad_sq);
-      err = cudaGetLastError();
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)tab.n);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = 0;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      err = cudaLaunchKernelEx(&cfg, lst_grad_sq_reduce_kernel, t, static_cast<const double*>(partials), grad_sq);
       if (err != cudaSuccess) return err;
     }
   }
