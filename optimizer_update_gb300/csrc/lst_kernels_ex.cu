@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads) lst_grad_sq_reduce_kernel(const __gr
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int c = threadIdx.x + k * kThreads;
-    a[k] = c < t.partials_per_run ? p[c] : 0.0;
+    a[k] = c < t.partials_per_run ? __ldcg(p + c) : 0.0;  // from L2: written by the other grid
   }
   const double x = warp_sum_f64((a[0] + a[1]) + (a[2] + a[3]));
   if ((threadIdx.x & 31) == 0) warp_total[threadIdx.x >> 5] = x;
@@ -150,8 +150,8 @@ __global__ void __launch_bounds__(kThreads) lst_grad_sq_reduce_kernel(const __gr
 // (fraction of the measured copy bandwidth, 1.1 G elements): the 12 B layout
 // is held to 3 resident CTAs of 256 threads per SM (0.957, against 0.832
 // uncapped and 0.888 with one task at a time); the 16 B layouts ask for no
-// minimum (0: 94 registers, 0.963; a minimum of one CTA per SM let the
-// compiler take 112 and measured 0.922).
+// minimum (0: about 90-98 registers, 2 CTAs per SM, 0.963; a minimum of one
+// CTA per SM let the compiler take 112 and measured 0.922).
 template <int FMT, bool GSQ>
 __global__ void __launch_bounds__(kThreads, (FMT == F_L12 ? 3 : 0))
     lst_update_ex_kernel(const __grid_constant__ RunTableEx tab, const Scalars s0, double* partials) {
