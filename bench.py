@@ -269,6 +269,61 @@ def cpu_oracle_rate(L, arrs, hp_kw, budget_s: float, threads: int):
         step += 1
 
 
+def parity_sample(L, arrs, hp_kw, device, threads: int, t: int = 7):
+    """One block of the current state stepped once by the product kernel (a
+    one-block layout with the block's geometry, lst_adamw_step) and once by
+    the oracle on a host copy: the largest fp32 relative error, the largest
+    bf16 distance in ulps, and whether every byte matches. Part of the CPU
+    baseline leg (the one place the bench may run the oracle besides the
+    reference arm)."""
+    import numpy as np
+    import torch
+    import oracle
+    from optimizer_update_gb300 import Layout, lst
+    i = max(range(L.n_layers), key=lambda k: (L.block(k)[1] if k else -1))  # the largest block but the first
+    Li = Layout([(name, (n,), 0) for (name, _off, n) in L.spans(i)], L.fmt)
+    if Li.block_bytes(0) != L.block_bytes(i):
+        return None
+    host = arrs[i].copy()
+    dev = torch.from_numpy(host).to(device)
+    lst.lst_adamw_step(Li.handle, [dev.data_ptr()], lst.adamw_hparams(step=t, **hp_kw),
+                       torch.cuda.current_stream(device).cuda_stream)
+    got = dev.cpu().numpy()
+    oracle.step(L.fmt, Li.numpy_views(0, host), oracle.hparams(step=t, **hp_kw), threads=threads)
+    gv, ev = Li.numpy_views(0, got), Li.numpy_views(0, host)
+    out = {"block": i, "elements": int(Li.block(0)[1]), "step": t, "bit_exact": bool(np.array_equal(got, host))}
+    rel, ulp, nans = 0.0, 0, 0
+
+    def order(x):  # bf16 bit patterns in monotone integer order
+        x = x.view(np.uint16).astype(np.int32)
+        return np.where(x & 0x8000, 0x8000 - (x & 0x7FFF), x + 0x8000)
+
+    for f, dt in Li.fields().items():
+        if f == "G":
+            continue
+        a, b = gv[f], ev[f]
+        if dt == "f32":
+            an, bn = np.isnan(a), np.isnan(b)
+        else:
+            an, bn = (a.view(np.uint16) & 0x7FFF) > 0x7F80, (b.view(np.uint16) & 0x7FFF) > 0x7F80
+        nans += int(bn.sum())
+        if not np.array_equal(an, bn):  # NaN on one side only
+            rel, ulp = float("inf"), 1 << 16
+            continue
+        a, b = a[~an], b[~bn]
+        if not a.size:
+            continue
+        if dt == "f32":
+            d = np.abs(a.astype(np.float64) - b.astype(np.float64)) / np.maximum(np.abs(b.astype(np.float64)), 1e-30)
+            rel = max(rel, float(np.max(d)))
+        else:
+            ulp = max(ulp, int(np.max(np.abs(order(a) - order(b)))))
+    out["max_rel_err_fp32"] = rel
+    out["max_ulp_bf16"] = ulp
+    out["nan_outputs"] = nans
+    return out
+
+
 # ---------------------------------------------------------------------------
 def run_reference(args):
     """The oracle alone, on the host cores: each step a bounded sample of the
@@ -361,9 +416,15 @@ def block_h2d_rates(torch, arrs, dev):
 
 def link_bandwidth(torch, host_ptr_arrs, dev_a, dev_b, nbytes: int, reps: int = 5):
     """Pinned host <-> device copy bandwidth: H2D alone, D2H alone, both at once
-    (each direction timed on its own stream with CUDA events)."""
+    (each direction timed on its own stream with CUDA events), on the given
+    host arrays (blocks of the state: the rate is the one the state's own
+    memory gets). The device-to-host direction writes back into the state, so
+    dev_b first receives a copy of exactly those bytes: every timed copy
+    rewrites the bytes that are already there."""
     h_in = torch.from_numpy(host_ptr_arrs[0][:nbytes])
     h_out = torch.from_numpy(host_ptr_arrs[1][:nbytes])
+    dev_b[:nbytes].copy_(h_out)
+    torch.cuda.synchronize()
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
 
     def timed(h2d: bool, d2h: bool):
@@ -616,12 +677,13 @@ def run_ours(args):
         store = run_store_leg(args, L, ptrs, buf0, buf1, hp_kw, device, world, rank)
 
     # ---- CPU baseline: the oracle on the host cores, bounded sample ------------
-    cpu = None
+    cpu, parity = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         rate, done, el, nblocks = cpu_oracle_rate(L, arrs, hp_kw, args.cpu_budget_s, threads)
         cpu = {"value": rate, "unit": "params/s", "cores": threads, "kind": "oracle",
                "sample": f"{nblocks} block updates ({done} params) of this workload's state in {el:.1f} s"}
+        parity = parity_sample(L, arrs, hp_kw, device, threads)
 
     for p in ptrs:
         lst.lst_host_free(p)
@@ -648,6 +710,7 @@ def run_ours(args):
             "stream_devgrad": stream_devgrad,
             **({"store": store} if store is not None else {}),
             "cpu_baseline": cpu,
+            "parity": parity,
             "clocks": clk,
             "gpu_launches": args.steps,
         }
