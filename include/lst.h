@@ -164,6 +164,22 @@ LST_API lst_status lst_layout_transfer(const lst_layout* layout, int64_t layer, 
    time (a multiple of 2048; 0 = one chunk per block). Default 16,777,216. */
 LST_API lst_status lst_layout_set_stream_chunk(lst_layout* layout, int64_t elems);
 
+/* How the streamed steps (lst_stream_step and its variants) move sub-chunks,
+   per direction (the pages' StreamIn / StreamOut):
+     LST_COPY_ENGINE  cudaMemcpyAsync / cudaMemcpy2DAsync on the copy engines;
+     LST_COPY_SM      a copy kernel on the same stream that reads or writes the
+                      host block through its device mapping (pinned memory
+                      registered as mapped, e.g. from lst_host_alloc).
+   A host block without a device mapping is moved by the copy engines. Both
+   give identical bytes. Default: LST_COPY_ENGINE both ways (on GB300 the
+   fastest pipeline on a host whose pinned memory copies at the link rate: the
+   copy kernels compete with the update kernel for the SMs). On a host where
+   the copy engines read some pinned allocations at a few GB/s, LST_COPY_SM
+   both ways was several times faster; lst_zero_copy_step faster still.
+   LST_ERR_INVALID_ARG for another value. */
+typedef enum { LST_COPY_ENGINE = 0, LST_COPY_SM = 1 } lst_copy_mode;
+LST_API lst_status lst_layout_set_stream_copy(lst_layout* layout, int32_t h2d_mode, int32_t d2h_mode);
+
 /* ------------------------------------------------------------------------
  * Device-resident step.
  * ------------------------------------------------------------------------ */

@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liblst.so")
 
-SOURCES = ["lst_layout.cpp", "lst_api.cpp", "lst_stream.cpp", "lst_store.cpp", "lst_kernels.cu", "lst_kernels_ex.cu", "lst_noalloc.cu"]
+SOURCES = ["lst_layout.cpp", "lst_api.cpp", "lst_stream.cpp", "lst_store.cpp", "lst_kernels.cu", "lst_kernels_ex.cu", "lst_noalloc.cu", "lst_copy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

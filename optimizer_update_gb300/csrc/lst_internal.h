@@ -55,6 +55,8 @@ struct lst_layout {
   int64_t n_params = 0;
   int64_t max_block_bytes = 0;
   int64_t stream_chunk = lst::kDefaultStreamChunk;
+  int stream_copy_h2d = LST_COPY_ENGINE;  // how the streamed steps move sub-chunks in
+  int stream_copy_d2h = LST_COPY_ENGINE;  // ... and out (lst_layout_set_stream_copy)
   std::vector<lst::Block> blocks;
   std::vector<lst::Tensor> tensors;
   std::mutex stream_mu;           // serialises lst_stream_step on this layout
@@ -92,6 +94,10 @@ Run block_run(const lst_layout& L, const Block& b, char* base, int64_t e0, int64
 
 // Enqueue the update over `runs` on `stream` (one launch per kMaxRunsPerLaunch
 // runs). Returns the first CUDA error, cudaSuccess otherwise.
+// SM copy of rows x row_bytes at the same pitch on both sides (lst_copy.cu).
+cudaError_t launch_stream_copy(const void* src, void* dst, size_t row_bytes, size_t pitch, int rows,
+                               cudaStream_t stream);
+
 cudaError_t launch_update(lst_format fmt, bool sgd, const Run* runs, int n_runs, const Scalars& s,
                           cudaStream_t stream);
 

@@ -224,6 +224,18 @@ extern "C" lst_status lst_layout_transfer(const lst_layout* L, int64_t layer, in
   return LST_OK;
 }
 
+extern "C" lst_status lst_layout_set_stream_copy(lst_layout* L, int32_t h2d_mode, int32_t d2h_mode) {
+  clear_error();
+  if (!L) return fail(LST_ERR_INVALID_ARG, "lst_layout_set_stream_copy: null layout");
+  auto ok = [](int32_t m) { return m == LST_COPY_ENGINE || m == LST_COPY_SM; };
+  if (!ok(h2d_mode) || !ok(d2h_mode))
+    return fail(LST_ERR_INVALID_ARG, "lst_layout_set_stream_copy: mode must be LST_COPY_ENGINE or LST_COPY_SM");
+  std::lock_guard<std::mutex> g(L->stream_mu);
+  L->stream_copy_h2d = h2d_mode;
+  L->stream_copy_d2h = d2h_mode;
+  return LST_OK;
+}
+
 extern "C" lst_status lst_layout_set_stream_chunk(lst_layout* L, int64_t elems) {
   clear_error();
   if (!L) return fail(LST_ERR_INVALID_ARG, "lst_layout_set_stream_chunk: null layout");

@@ -122,6 +122,16 @@ static cudaError_t do_copy2d(void* p) {
   Copy2DOp* c = static_cast<Copy2DOp*>(p);
   return cudaMemcpy2DAsync(c->dst, c->pitch, c->src, c->pitch, c->width, c->rows, c->dir, c->st);
 }
+struct SmCopyOp {  // the same rows moved by the SMs (lst_copy.cu)
+  void* dst;
+  const void* src;
+  size_t pitch, width, rows;
+  cudaStream_t st;
+};
+static cudaError_t do_sm_copy(void* p) {
+  SmCopyOp* c = static_cast<SmCopyOp*>(p);
+  return launch_stream_copy(c->src, c->dst, c->width, c->pitch, (int)c->rows, c->st);
+}
 struct RecordOp {
   cudaEvent_t ev;
   cudaStream_t st;
@@ -196,7 +206,7 @@ static std::vector<int64_t> chunk_cuts(int64_t padded, int64_t C, bool first_blo
 // device's limit.
 static cudaError_t enqueue_range(Enqueuer& enq, const Engine* E, const FormatInfo& fi, const Block& b, int k0, int k1,
                                  int64_t e0, int64_t e1, char* to, const char* from, cudaMemcpyKind dir,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, bool sm) {
   int k = k0;
   while (k < k1) {
     const int64_t eb = fi.elem_bytes[k];
@@ -207,7 +217,11 @@ static cudaError_t enqueue_range(Enqueuer& enq, const Engine* E, const FormatInf
       ++k2;
     const int64_t off = b.seg_off[fi.field[k]] + e0 * eb;
     const size_t width = (size_t)((e1 - e0) * eb);
-    if (k2 - k > 1 && pitch <= E->max_pitch) {
+    if (sm) {  // one launch for the group, any pitch
+      SmCopyOp c{to + off, from + off, pitch, width, (size_t)(k2 - k), st};
+      cudaError_t err = enq(do_sm_copy, &c);
+      if (err != cudaSuccess) return err;
+    } else if (k2 - k > 1 && pitch <= E->max_pitch) {
       Copy2DOp c{to + off, from + off, pitch, width, (size_t)(k2 - k), dir, st};
       cudaError_t err = enq(do_copy2d, &c);
       if (err != cudaSuccess) return err;
@@ -276,7 +290,9 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
         return fail(LST_ERR_ALIGNMENT, "lst_stream_step: gradient of block %lld not 16-byte aligned", (long long)i);
     }
   }
-  // Pinned / device checks (host-side driver queries, no device work).
+  // Pinned / device checks (host-side driver queries, no device work), and
+  // each host block's device mapping for the SM copies (null: none).
+  std::vector<char*> mapped((size_t)n, nullptr);
   for (int64_t i = 0; i < n; ++i) {
     if (L->blocks[(size_t)i].bytes == 0 || skipped(i)) continue;
     cudaPointerAttributes a;
@@ -288,6 +304,7 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
     if (a.type != cudaMemoryTypeHost)
       return fail(LST_ERR_NOT_PINNED, "lst_stream_step: host block %lld is not pinned host memory",
                   (long long)i);
+    mapped[(size_t)i] = static_cast<char*>(a.devicePointer);
   }
   for (void* d : {dev_buf0, dev_buf1}) {
     cudaPointerAttributes a;
@@ -348,6 +365,11 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
     const int bi = (int)(i & 1);
     char* buf = bufs[bi];
     char* host = static_cast<char*>(host_blocks[i]);
+    // the SMs reach the host block through its device mapping
+    const bool sm_in = L->stream_copy_h2d == LST_COPY_SM && mapped[(size_t)i];
+    const bool sm_out = L->stream_copy_d2h == LST_COPY_SM && mapped[(size_t)i];
+    char* host_in = sm_in ? mapped[(size_t)i] : host;
+    char* host_out = sm_out ? mapped[(size_t)i] : host;
     if (used[bi]) {  // buffer-free: the last outbound copy from this buffer
       RecordOp w{E->buffer_free[bi], E->h2d};
       if ((err = enq(do_wait, &w)) != cudaSuccess) { what = "wait buffer-free"; break; }
@@ -363,10 +385,18 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
       const int first_in = dev_grads ? 1 : 0;
       if (whole) {
         const int64_t off = b.seg_off[fi.field[first_in]];
-        CopyOp c{buf + off, host + off, (size_t)(b.h2d_off + b.h2d_bytes - off), cudaMemcpyHostToDevice, E->h2d};
-        if ((err = enq(do_copy, &c)) != cudaSuccess) { what = "copy in"; break; }
+        const size_t nb = (size_t)(b.h2d_off + b.h2d_bytes - off);
+        if (sm_in) {
+          SmCopyOp c{buf + off, host_in + off, nb, nb, 1, E->h2d};
+          err = enq(do_sm_copy, &c);
+        } else {
+          CopyOp c{buf + off, host + off, nb, cudaMemcpyHostToDevice, E->h2d};
+          err = enq(do_copy, &c);
+        }
+        if (err != cudaSuccess) { what = "copy in"; break; }
       } else {
-        err = enqueue_range(enq, E, fi, b, first_in, fi.n_inputs, e0, e1, buf, host, cudaMemcpyHostToDevice, E->h2d);
+        err = enqueue_range(enq, E, fi, b, first_in, fi.n_inputs, e0, e1, buf, host_in, cudaMemcpyHostToDevice,
+                            E->h2d, sm_in);
         if (err != cudaSuccess) { what = "copy in"; break; }
       }
       RecordOp r1{E->weights_ready[bi], E->h2d};
@@ -389,11 +419,18 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
       if ((err = enq(do_wait, &w2)) != cudaSuccess) { what = "wait update-done"; break; }
       // StreamOut: the fields the update wrote.
       if (whole) {
-        CopyOp c{host + b.d2h_off, buf + b.d2h_off, (size_t)b.d2h_bytes, cudaMemcpyDeviceToHost, E->d2h};
-        if ((err = enq(do_copy, &c)) != cudaSuccess) { what = "copy out"; break; }
+        const size_t nb = (size_t)b.d2h_bytes;
+        if (sm_out) {
+          SmCopyOp c{host_out + b.d2h_off, buf + b.d2h_off, nb, nb, 1, E->d2h};
+          err = enq(do_sm_copy, &c);
+        } else {
+          CopyOp c{host + b.d2h_off, buf + b.d2h_off, nb, cudaMemcpyDeviceToHost, E->d2h};
+          err = enq(do_copy, &c);
+        }
+        if (err != cudaSuccess) { what = "copy out"; break; }
       } else {
-        err = enqueue_range(enq, E, fi, b, fi.first_output, fi.n_segments, e0, e1, host, buf, cudaMemcpyDeviceToHost,
-                            E->d2h);
+        err = enqueue_range(enq, E, fi, b, fi.first_output, fi.n_segments, e0, e1, host_out, buf,
+                            cudaMemcpyDeviceToHost, E->d2h, sm_out);
         if (err != cudaSuccess) { what = "copy out"; break; }
       }
     }

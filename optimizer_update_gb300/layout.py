@@ -78,6 +78,10 @@ class Layout:
     def set_stream_chunk(self, elems: int) -> None:
         lst.lst_layout_set_stream_chunk(self.handle, elems)
 
+    def set_stream_copy(self, h2d_mode: int, d2h_mode: int) -> None:
+        """lst.LST_COPY_ENGINE or lst.LST_COPY_SM for each direction of the streamed steps."""
+        lst.lst_layout_set_stream_copy(self.handle, h2d_mode, d2h_mode)
+
     # views ------------------------------------------------------------------
     def numpy_views(self, layer: int, buf):
         """Field -> numpy view over a host block (a uint8 numpy array of the block's size)."""

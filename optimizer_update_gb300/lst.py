@@ -100,6 +100,7 @@ def lib() -> ctypes.CDLL:
             "lst_layout_tensor": ([vp, i32, i32, P(i64), P(i64), P(i64)], ctypes.c_int),
             "lst_layout_transfer": ([vp, i64, P(i64), P(i64), P(i64), P(i64)], ctypes.c_int),
             "lst_layout_set_stream_chunk": ([vp, i64], ctypes.c_int),
+            "lst_layout_set_stream_copy": ([vp, i32, i32], ctypes.c_int),
             "lst_adamw_step": ([vp, P(vp), P(lst_adamw_hparams), vp], ctypes.c_int),
             "lst_sgd_step": ([vp, P(vp), f32, vp], ctypes.c_int),
             "lst_stream_step": ([vp, P(vp), vp, vp, P(lst_adamw_hparams), i64], ctypes.c_int),
@@ -205,6 +206,13 @@ def lst_layout_transfer(handle: int, layer: int) -> Tuple[int, int, int, int]:
 
 def lst_layout_set_stream_chunk(handle: int, elems: int) -> None:
     _check(lib().lst_layout_set_stream_chunk(handle, elems))
+
+
+LST_COPY_ENGINE, LST_COPY_SM = 0, 1
+
+
+def lst_layout_set_stream_copy(handle: int, h2d_mode: int, d2h_mode: int) -> None:
+    _check(lib().lst_layout_set_stream_copy(handle, h2d_mode, d2h_mode))
 
 
 def lst_adamw_step(handle: int, dev_blocks: Sequence[int], hparams: lst_adamw_hparams, stream: int = 0) -> None:

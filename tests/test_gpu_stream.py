@@ -40,9 +40,11 @@ def _bufs(L):
     return b0, b1
 
 
-def _stream_vs_device(specs, fmt, workload, t, chunk, steps=1):
+def _stream_vs_device(specs, fmt, workload, t, chunk, steps=1, copy=None):
     L = Layout(specs, fmt)
     L.set_stream_chunk(chunk)
+    if copy is not None:
+        L.set_stream_copy(*copy)
     P = PinnedBlocks(L)
     try:
         for i in range(L.n_layers):
@@ -86,6 +88,24 @@ def test_stream_bit_identical_small_chunks(fmt, workload, chunk):
     specs = [("a", (70_001,), 0), ("b", (4097,), 1), ("c", (30_000,), 1), ("d", (9,), 2), ("e", (2048,), 3),
              ("f", (12_288,), 4)]
     _stream_vs_device(specs, fmt, workload, 3, chunk, steps=3)
+
+
+E, SM = lst.LST_COPY_ENGINE, lst.LST_COPY_SM
+
+
+@pytest.mark.parametrize("fmt,workload", FMTS)
+@pytest.mark.parametrize("copy", [(E, E), (SM, E), (E, SM), (SM, SM)], ids=["ce-ce", "sm-ce", "ce-sm", "sm-sm"])
+def test_stream_copy_modes_bit_identical(fmt, workload, copy):
+    """Sub-chunks moved by the copy engines or by the SM copy kernel, in either
+    direction: the same bytes as the device-resident step."""
+    _stream_vs_device(_three_tinyllama_layers(), fmt, workload, 10, 1 << 20, steps=2, copy=copy)
+
+
+@pytest.mark.parametrize("fmt,workload", FMTS)
+@pytest.mark.parametrize("chunk", [0, 6144])
+def test_stream_sm_copies_whole_blocks_and_ragged_chunks(fmt, workload, chunk):
+    specs = [("a", (70_001,), 0), ("b", (4097,), 1), ("c", (30_000,), 1), ("d", (9,), 2), ("e", (2048,), 3)]
+    _stream_vs_device(specs, fmt, workload, 3, chunk, steps=2, copy=(SM, SM))
 
 
 def test_stream_lora_many_small_blocks():
