@@ -414,6 +414,42 @@ def block_h2d_rates(torch, arrs, dev):
     return out
 
 
+def heal_pinned_state(torch, L, ptrs, arrs, dev, tries: int = 3, max_extra_bytes: int = 40 << 30):
+    """Health check of the pinned state blocks. On the GB300 hosts here, some
+    pinned allocations are read by the copy engines at a few GB/s instead of
+    the link rate, for their whole lifetime (more of them after other
+    processes have pinned and freed a lot of memory). A block whose
+    host-to-device rate is under half the best block's is copied into a fresh
+    allocation, up to `tries` times; replaced allocations stay pinned until
+    the caller frees them (returned), so the allocator does not hand the same
+    pages straight back. Returns (slow blocks before, blocks replaced,
+    allocations to free)."""
+    import ctypes
+    import numpy as np
+    from optimizer_update_gb300 import lst
+    rates = block_h2d_rates(torch, arrs, dev)
+    ref = max(rates)
+    slow_before = sum(1 for r in rates if r < 0.5 * ref)
+    retired, healed, extra = [], 0, 0
+    for i, r in enumerate(rates):
+        k = 0
+        while r < 0.5 * ref and k < tries:
+            n = arrs[i].size
+            if extra + n > max_extra_bytes:
+                break
+            p = lst.lst_host_alloc(n)
+            a = np.ctypeslib.as_array((ctypes.c_uint8 * n).from_address(p))
+            a[:] = arrs[i]
+            retired.append(ptrs[i])
+            ptrs[i], arrs[i] = p, a
+            extra += n
+            r = block_h2d_rates(torch, [a], dev)[0]
+            k += 1
+        if k:
+            healed += 1
+    return slow_before, healed, retired
+
+
 def link_bandwidth(torch, host_ptr_arrs, dev_a, dev_b, nbytes: int, reps: int = 5):
     """Pinned host <-> device copy bandwidth: H2D alone, D2H alone, both at once
     (each direction timed on its own stream with CUDA events), on the given
@@ -569,6 +605,9 @@ def run_ours(args):
     a0 = arrs[big[0]] if big else arrs[0]
     a1 = arrs[big[-1]] if len(big) > 1 else arrs[-1]
     nb = min(a0.size, a1.size, buf0.numel(), 1 << 30)
+    slow_before_heal, healed, retired = heal_pinned_state(torch, L, ptrs, arrs, buf0)
+    a0 = arrs[big[0]] if big else arrs[0]
+    a1 = arrs[big[-1]] if len(big) > 1 else arrs[-1]
     link = link_bandwidth(torch, [a0, a1], buf0, buf1, nb)
 
     # ---- streamed leg (the public end-to-end call) ------------------------------
@@ -619,7 +658,8 @@ def run_ours(args):
                        chunk_elems=chunk, warmup_steps=stream_warm,
                        host_huge_page_bytes=huge_bytes, host_state_bytes=state_bytes,
                        block_h2d_gbs_min=min(block_rates), block_h2d_gbs_median=statistics.median(block_rates),
-                       slow_blocks=sum(1 for r in block_rates if r < 0.5 * link["h2d_gbs"]))
+                       slow_blocks=sum(1 for r in block_rates if r < 0.5 * link["h2d_gbs"]),
+                       slow_blocks_before_heal=slow_before_heal, healed_blocks=healed)
 
     # ---- streamed leg with device-resident gradients: only the state crosses
     # the link inbound (the gradients stand for what a backward pass leaves on
@@ -685,7 +725,7 @@ def run_ours(args):
                "sample": f"{nblocks} block updates ({done} params) of this workload's state in {el:.1f} s"}
         parity = parity_sample(L, arrs, hp_kw, device, threads)
 
-    for p in ptrs:
+    for p in ptrs + retired:
         lst.lst_host_free(p)
 
     if rank == 0:
