@@ -106,6 +106,39 @@ def max_over_ranks(x: float, device=None) -> float:
     return float(t.item())
 
 
+def sum_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def shard_blocks(block_bytes, world: int):
+    """Contiguous block ranges [start, stop) of one model for `world` ranks,
+    balanced by bytes: rank r's range ends at the block boundary nearest to
+    (r + 1) / world of the model's bytes (every rank gets at least one block
+    while there are blocks enough; ranges may be empty when there are fewer
+    blocks than ranks). The update needs no exchange between ranks."""
+    n = len(block_bytes)
+    total = float(sum(block_bytes))
+    cum = [0.0]
+    for b in block_bytes:
+        cum.append(cum[-1] + b)
+    cuts = [0]
+    for r in range(1, world):
+        target = total * r / world
+        k = min(range(cuts[-1], n + 1), key=lambda j: (abs(cum[j] - target), j))
+        # leave at least one block for each remaining rank when possible
+        k = max(k, min(cuts[-1] + 1, n))
+        k = min(k, max(n - (world - r), cuts[-1]))
+        cuts.append(k)
+    cuts.append(n)
+    return [(cuts[r], cuts[r + 1]) for r in range(world)]
+
+
 def replica_seed(seed: int, rank: int) -> int:
     """Each rank's replica draws its own state (weak scaling: a disjoint shard
     of an N-times larger job)."""
@@ -212,16 +245,35 @@ def kernel_traffic(kernel: str, fmt: str, params: int):
     return per_param * params
 
 
-def build_layout(workload: str, max_blocks: int = 0):
-    """The workload's layout; max_blocks > 0 keeps only its first blocks (a
-    smaller case of the same kernel, e.g. for profiling)."""
+def workload_specs(workload: str, max_blocks: int = 0):
+    """(tensor name, shape, block) of the workload; max_blocks > 0 keeps only
+    its first blocks (a smaller case of the same kernel, e.g. for profiling)."""
     from synth import shapes
-    from optimizer_update_gb300 import Layout
-    fn, fmt, _ = WORKLOADS[workload]
+    fn, _, _ = WORKLOADS[workload]
     specs = getattr(shapes, fn)()
     if max_blocks > 0:
         specs = [s for s in specs if s[2] < max_blocks]
-    return Layout(specs, fmt)
+    return specs
+
+
+def build_layout(workload: str, max_blocks: int = 0):
+    from optimizer_update_gb300 import Layout
+    return Layout(workload_specs(workload, max_blocks), WORKLOADS[workload][1])
+
+
+def rank_layout(workload: str, max_blocks: int, shard: bool, rank: int, world: int):
+    """The layout this rank updates and the model index of its first block:
+    the whole model (a replica), or with `shard` its contiguous range of the
+    model's blocks (shard_blocks)."""
+    from optimizer_update_gb300 import Layout
+    full = build_layout(workload, max_blocks)
+    if not shard or world == 1:
+        return full, 0
+    a, b = shard_blocks([full.block_bytes(i) for i in range(full.n_layers)], world)[rank]
+    if a == b:
+        raise SystemExit(f"--shard: {full.n_layers} blocks cannot give rank {rank} of {world} a block")
+    specs = [(n, sh, blk - a) for (n, sh, blk) in workload_specs(workload, max_blocks) if a <= blk < b]
+    return Layout(specs, full.fmt), a
 
 
 def anon_huge_page_bytes() -> int:
@@ -236,7 +288,9 @@ def anon_huge_page_bytes() -> int:
     return 0
 
 
-def alloc_pinned_state(L, workload: str, seed: int):
+def alloc_pinned_state(L, workload: str, seed: int, first_block: int = 0):
+    """Pinned host blocks drawn from the generator; block i of L is block
+    first_block + i of the model (a shard draws the model's own blocks)."""
     import ctypes
     import numpy as np
     import synth
@@ -246,7 +300,7 @@ def alloc_pinned_state(L, workload: str, seed: int):
         n = L.block_bytes(i)
         p = lst.lst_host_alloc(n)
         a = np.ctypeslib.as_array((ctypes.c_uint8 * n).from_address(p))
-        synth.fill_block(L.numpy_views(i, a), L.spans(i), i, workload, L.fmt, t=1, seed=seed)
+        synth.fill_block(L.numpy_views(i, a), L.spans(i), first_block + i, workload, L.fmt, t=1, seed=seed)
         ptrs.append(p)
         arrs.append(a)
     return ptrs, arrs
@@ -383,15 +437,19 @@ def run_reference(args):
     return 0
 
 
-def config_for(L, workload, world, max_blocks=0):
+def config_for(L, workload, world, max_blocks=0, shard=False, params_job=None):
     desc = WORKLOADS[workload][2]
     if max_blocks > 0:
-        desc += f", first {L.n_layers} blocks only"
+        desc += f", first {max_blocks} blocks only"
     state = sum(L.block_bytes(i) for i in range(L.n_layers))
     l2 = "inputs larger than twice the L2 (no flush)" if state >= 2 * (132 << 20) else \
         "L2 flushed before every timed launch (a write of twice its size, then a read of another such buffer)"
-    return {"workload": desc, "name": workload, "layout": L.fmt, "params": L.n_params,
-            "blocks": L.n_layers, "state_bytes": state, "l2": l2, "parallelism": f"replicas x{world}",
+    sharded = shard and world > 1
+    return {"workload": desc, "name": workload, "layout": L.fmt,
+            "params": int(params_job) if sharded and params_job else L.n_params,
+            "blocks": L.n_layers, "state_bytes": state, "l2": l2,
+            "parallelism": (f"blocks sharded x{world} (rank 0: {L.n_layers} blocks, {L.n_params} params)" if sharded
+                            else f"replicas x{world}"),
             "hparams": HP_LORA if L.fmt == "L16F" else HP}
 
 
@@ -501,14 +559,16 @@ def run_ours(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     dist_init("nccl")
-    seed = replica_seed(args.seed, rank)
+    # replicas draw their own state; shards are parts of one model (one seed)
+    seed = args.seed if args.shard else replica_seed(args.seed, rank)
 
-    L = build_layout(args.workload, args.max_blocks)
+    L, first_block = rank_layout(args.workload, args.max_blocks, args.shard, rank, world)
     hp_kw = HP_LORA if L.fmt == "L16F" else HP
     P = L.n_params
+    P_job = sum_over_ranks(P, device)  # parameters all ranks update per step
     chunk = 1 << 24  # 16 Mi elements per sub-chunk (the library default)
     L.set_stream_chunk(chunk)
-    ptrs, arrs = alloc_pinned_state(L, args.workload, seed)
+    ptrs, arrs = alloc_pinned_state(L, args.workload, seed, first_block)
     huge_bytes = anon_huge_page_bytes()  # the pinned blocks' share of huge pages
 
     # ---- device-resident leg -------------------------------------------------
@@ -563,7 +623,7 @@ def run_ours(args):
     per_launch = [starts[k].elapsed_time(ends[k]) / 1e3 for k in range(args.steps)]
     t_dev = sum(per_launch)
     t_dev_max = max_over_ranks(t_dev, device)
-    value = world * P * args.steps / t_dev_max
+    value = P_job * args.steps / t_dev_max
     avg_launch = t_dev / args.steps
     alg_bytes = ALG_BYTES[L.fmt] * P
     peak, peak_kind = measured_peaks()
@@ -645,7 +705,7 @@ def run_ours(args):
         t += 1
     t_e2e = time.perf_counter() - t0
     t_e2e_max = max_over_ranks(t_e2e, device)
-    e2e_value = world * P * e_steps / t_e2e_max
+    e2e_value = P_job * e_steps / t_e2e_max
     chunks = sum((L.padded(i) + chunk - 1) // chunk for i in range(L.n_layers))
     roof_t = max(h2d_b / (link["h2d_concurrent_gbs"] * 1e9), d2h_b / (link["d2h_concurrent_gbs"] * 1e9))
     # the same bytes with the two directions one after the other (each at its
@@ -683,7 +743,7 @@ def run_ours(args):
         t += 1
     t_dg = max_over_ranks(time.perf_counter() - t0, device)
     roof_dg = max(dg_h2d / (link["h2d_concurrent_gbs"] * 1e9), d2h_b / (link["d2h_concurrent_gbs"] * 1e9))
-    stream_devgrad = {"value": world * P * e_steps / t_dg, "unit": "params/s", "call": "lst_stream_step_devgrad",
+    stream_devgrad = {"value": P_job * e_steps / t_dg, "unit": "params/s", "call": "lst_stream_step_devgrad",
                       "step_ms": 1e3 * t_dg / e_steps, "h2d_bytes_per_step": dg_h2d, "d2h_bytes_per_step": d2h_b,
                       "roofline_ms": 1e3 * roof_dg, "frac_of_link_roofline": roof_dg / (t_dg / e_steps),
                       "steps": e_steps, "warmup_steps": devgrad_warm}
@@ -707,7 +767,7 @@ def run_ours(args):
     link_after = link_bandwidth(torch, [a0, a1], buf0, buf1, nb)
     stream_info["link_after"] = {k: link_after[k] for k in ("h2d_gbs", "d2h_gbs", "h2d_concurrent_gbs",
                                                              "d2h_concurrent_gbs")}
-    zero_copy = {"value": world * P * e_steps / t_zc, "unit": "params/s", "call": "lst_zero_copy_step",
+    zero_copy = {"value": P_job * e_steps / t_zc, "unit": "params/s", "call": "lst_zero_copy_step",
                  "step_ms": 1e3 * t_zc / e_steps, "link_bytes_per_step": h2d_b + d2h_b,
                  "frac_of_link_roofline": roof_t / (t_zc / e_steps), "steps": e_steps, "warmup_steps": zc_warm}
 
@@ -732,8 +792,9 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * t_dev_max / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": config_for(L, args.workload, world, args.max_blocks),
+            "scaling": "strong" if (args.shard and world > 1) else "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": config_for(L, args.workload, world, args.max_blocks, args.shard, P_job),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": f"{kname}<{L.fmt}>", "alg_bytes_per_launch": alg_bytes,
@@ -808,7 +869,7 @@ def time_options_leg(args, L, dptrs, hp_kw, stream, device, world, t, flush, flu
     avg = sum(per) / k_steps
     achieved = ALG_BYTES[L.fmt] * L.n_params / avg / 1e9
     finite = bool(torch.isfinite(gsq).all().item()) and bool((gsq > 0).all().item())
-    return {"value": world * L.n_params * k_steps / t_max, "unit": "params/s", "call": "lst_adamw_step_ex",
+    return {"value": sum_over_ranks(L.n_params, device) * k_steps / t_max, "unit": "params/s", "call": "lst_adamw_step_ex",
             "per_block_steps": True, "grad_sq": True, "achieved_gbs": achieved, "frac_of_hbm_peak": achieved / peak,
             "avg_launch_ms": 1e3 * avg, "median_launch_ms": 1e3 * statistics.median(per), "steps": k_steps,
             "grad_sq_all_positive_finite": finite}
@@ -847,7 +908,7 @@ def time_sgd_leg(args, L, dptrs, hp_kw, stream, device, world, flush, flush_rd, 
     t_max = max_over_ranks(sum(per), device)
     avg = sum(per) / k_steps
     achieved = SGD_BYTES[L.fmt] * L.n_params / avg / 1e9
-    return {"value": world * L.n_params * k_steps / t_max, "unit": "params/s", "call": "lst_sgd_step",
+    return {"value": sum_over_ranks(L.n_params, device) * k_steps / t_max, "unit": "params/s", "call": "lst_sgd_step",
             "alg_bytes_per_param": SGD_BYTES[L.fmt], "achieved_gbs": achieved, "frac_of_hbm_peak": achieved / peak,
             "avg_launch_ms": 1e3 * avg, "median_launch_ms": 1e3 * statistics.median(per), "steps": k_steps}
 
@@ -919,7 +980,7 @@ def run_store_leg(args, L, ptrs, buf0, buf1, hp_kw, device, world, rank):
             lst.lst_host_free(p)
         shutil.rmtree(top, ignore_errors=True)
     serial = state / (w_gbs * 1e9) + state / (r_gbs * 1e9)
-    return {"value": world * L.n_params / dt, "unit": "params/s", "call": "lst_store_step", "step_s": dt,
+    return {"value": sum_over_ranks(L.n_params, device) / dt, "unit": "params/s", "call": "lst_store_step", "step_s": dt,
             "file_read_bytes_per_step": state, "file_write_bytes_per_step": state,
             "disk_write_gbs": w_gbs, "disk_read_gbs": r_gbs, "direct_io": direct,
             "disk_serial_s": serial, "frac_of_disk_serial": serial / dt,
@@ -938,6 +999,9 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shard", action="store_true",
+                    help="with N > 1: each rank updates a contiguous range of the model's blocks (strong scaling) "
+                         "instead of a replica of the whole model (weak scaling, the default)")
     ap.add_argument("--store-dir", default=None,
                     help="also time lst_store_step with the blocks in files under this directory (writes twice "
                          "the state to disk, removed afterwards)")
