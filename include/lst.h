@@ -268,8 +268,8 @@ LST_API lst_status lst_adamw_step_ex(const lst_layout* layout, void* const* dev_
    address (cudaGetSymbolAddress) with that device current; make that first
    call before any stream capture. The call allocates nothing: no cudaMalloc,
    no cudaFree, no allocating library routine.
-   All calls share the one array, which keeps the last call's contents; the
-   library zeroes what must start at zero before each launch. Calls whose
+   All calls share the one array, which keeps the last call's contents;
+   nothing in it needs to start at any value. Calls whose
    work overlaps on the GPU (streams with no ordering between them) race on
    the array: order them, or use lst_adamw_step_ex with separate workspaces.
    block_steps, skip: host arrays of n_layers entries, or NULL; grad_sq: a
@@ -295,8 +295,9 @@ LST_API lst_status lst_adamw_step_ex_noalloc(const lst_layout* layout, void* con
    For each block, in sub-chunks of the layout's stream chunk size: the input
    prefix is copied host -> device on a copy stream, the update runs on a
    compute stream, and the output suffix is copied device -> host on a second
-   copy stream; the streams wait only on events. Results are bit-identical to
-   lst_adamw_step on the same data.
+   copy stream; the streams wait only on events. The copies are copy-engine
+   transfers or, per lst_layout_set_stream_copy, an SM copy kernel on the same
+   copy stream. Results are bit-identical to lst_adamw_step on the same data.
    Synchronous: returns when all copies back to the host blocks are complete,
    or with LST_ERR_TIMEOUT once timeout_ms has passed (timeout_ms <= 0: no
    deadline); in that case work
