@@ -188,3 +188,32 @@ def test_step_options_validation_before_any_cuda_call(L):
         assert e.value.status == L.LST_ERR_INVALID_ARG
     finally:
         L.lst_layout_destroy(h)
+
+
+def test_bench_runs_the_oracle_only_in_its_baseline_and_reference_legs():
+    """bench.py imports the oracle only inside the CPU-baseline helpers and the
+    reference arm, and calls those helpers only from the baseline leg (rank 0,
+    one process, CPU baseline on) and from the reference entry."""
+    import ast
+    tree = ast.parse(open(os.path.join(ROOT, "bench.py")).read())
+    importers = set()
+    for fn in ast.walk(tree):
+        if isinstance(fn, ast.FunctionDef):
+            for node in ast.walk(fn):
+                if isinstance(node, ast.Import) and any(a.name.split(".")[0] == "oracle" for a in node.names):
+                    importers.add(fn.name)
+                if isinstance(node, ast.ImportFrom) and (node.module or "").split(".")[0] == "oracle":
+                    importers.add(fn.name)
+    assert importers == {"cpu_oracle_rate", "parity_sample", "run_reference"}
+    # no module-level import of the oracle
+    for node in tree.body:
+        if isinstance(node, (ast.Import, ast.ImportFrom)):
+            names = [a.name for a in node.names] + [getattr(node, "module", None) or ""]
+            assert not any(n.split(".")[0] == "oracle" for n in names)
+    # the baseline helpers are called only under the CPU-baseline condition
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    for helper in ("cpu_oracle_rate(", "parity_sample("):
+        calls = [i for i in range(len(src)) if src.startswith(helper, i) and not src[:i].endswith("def ")]
+        assert len(calls) == 1, helper
+        guard = src.rfind("if rank == 0 and world == 1 and not args.no_cpu_baseline:", 0, calls[0])
+        assert guard != -1 and calls[0] - guard < 600, helper
