@@ -673,10 +673,9 @@ def run_ours(args):
     # ---- streamed leg (the public end-to-end call) ------------------------------
     h2d_b = sum(L.transfer(i)[1] for i in range(L.n_layers))
     d2h_b = sum(L.transfer(i)[3] for i in range(L.n_layers))
-    # Host-link throughput on a shared host varies from moment to moment
-    # (single pinned copies measured at 57-150 GB/s instead of 210 now and
-    # then, whole steps several times slower than the roofline in such
-    # periods). Untimed warm-up steps until two in a row agree within 5 % (at
+    # On the shared hosts here, host-link throughput also varies from moment
+    # to moment (besides the slow allocations the health check above
+    # replaces). Untimed warm-up steps until two in a row agree within 5 % (at
     # least 3, at most 12); the link is measured again after the streamed legs.
     def warm(call):
         nonlocal t
@@ -697,12 +696,15 @@ def run_ours(args):
     # before the timed steps (a slow pinned allocation holds up the pipeline)
     block_rates = block_h2d_rates(torch, arrs, buf0)
     e_steps = max(1, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize(device)
     barrier(device)
+    torch.cuda.synchronize(device)
     t0 = time.perf_counter()
     for _ in range(e_steps):
         lst.lst_stream_step(L.handle, ptrs, buf0.data_ptr(), buf1.data_ptr(),
                             lst.adamw_hparams(step=t, **hp_kw), 600_000)
         t += 1
+    torch.cuda.synchronize(device)
     t_e2e = time.perf_counter() - t0
     t_e2e_max = max_over_ranks(t_e2e, device)
     e2e_value = P_job * e_steps / t_e2e_max
