@@ -37,6 +37,11 @@ int main(void) {
   void* blocks[2] = {0, 0};
   st = lst_adamw_step(L, blocks, &hp, NULL);
   printf("%d %s | %s\n", (int)st, lst_status_string(st), lst_last_error());
+  /* streamed-step settings: sub-chunk size and copy mode per direction */
+  int ok = lst_layout_set_stream_chunk(L, 4096) == LST_OK &&
+           lst_layout_set_stream_copy(L, LST_COPY_SM, LST_COPY_ENGINE) == LST_OK &&
+           lst_layout_set_stream_copy(L, 2, LST_COPY_ENGINE) == LST_ERR_INVALID_ARG;
+  printf("%d\n", ok);
   lst_layout_destroy(L);
   return 0;
 }
@@ -71,3 +76,4 @@ def test_c99_program_uses_the_abi(libdir, tmp_path):
     # master data starts after the bf16 G segment, 32 fp32 elements in
     assert nums[8:10] == [2 * 2048 + 32 * 4, 32]
     assert out[1].startswith("1 invalid argument")
+    assert out[2] == "1"
