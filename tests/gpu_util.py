@@ -36,21 +36,39 @@ def host_array(ptr: int, nbytes: int) -> np.ndarray:
 
 
 class PinnedBlocks:
-    """One page-locked host block per layer (lst_host_alloc)."""
+    """One page-locked host block per layer (lst_host_alloc). With guard > 0
+    (a multiple of 4096), each block sits between two canary bands of
+    `guard` bytes inside its allocation; guards_intact() checks them."""
 
-    def __init__(self, L: Layout):
+    def __init__(self, L: Layout, guard: int = 0):
+        assert guard % 4096 == 0
+        self.guard = guard
+        self._allocs: List[int] = []
+        self._full: List[np.ndarray] = []
         self.ptrs: List[int] = []
         self.arrays: List[np.ndarray] = []
         for i in range(L.n_layers):
             n = L.block_bytes(i)
-            p = lst.lst_host_alloc(n)
-            self.ptrs.append(p)
-            self.arrays.append(host_array(p, n))
+            base = lst.lst_host_alloc(n + 2 * guard)
+            self._allocs.append(base)
+            if guard:
+                full = host_array(base, n + 2 * guard)
+                full[:guard] = 0xA5
+                full[guard + n:] = 0x5A
+                self._full.append(full)
+            self.ptrs.append(base + guard)
+            self.arrays.append(host_array(base + guard, n))
+
+    def guards_intact(self) -> bool:
+        g = self.guard
+        return all(bool((f[:g] == 0xA5).all()) and bool((f[-g:] == 0x5A).all()) for f in self._full)
 
     def free(self) -> None:
         self.arrays = []
-        for p in self.ptrs:
+        self._full = []
+        for p in self._allocs:
             lst.lst_host_free(p)
+        self._allocs = []
         self.ptrs = []
 
 

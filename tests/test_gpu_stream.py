@@ -108,6 +108,36 @@ def test_stream_sm_copies_whole_blocks_and_ragged_chunks(fmt, workload, chunk):
     _stream_vs_device(specs, fmt, workload, 3, chunk, steps=2, copy=(SM, SM))
 
 
+@pytest.mark.parametrize("path", ["stream-ce", "stream-sm", "zero-copy"])
+def test_host_writes_stay_inside_the_blocks(path):
+    """Canary bands of 4 KB around every pinned host block stay untouched by
+    the paths that write host memory: copy-engine outbound copies, the SM copy
+    kernel, and the zero-copy kernel (ragged blocks, small chunks)."""
+    specs = [("a", (70_001,), 0), ("b", (4097,), 1), ("c", (9,), 2), ("d", (30_000,), 3)]
+    L = Layout(specs, "L16M")
+    L.set_stream_chunk(6144)
+    if path == "stream-sm":
+        L.set_stream_copy(SM, SM)
+    P = PinnedBlocks(L, guard=4096)
+    try:
+        for i in range(L.n_layers):
+            fill_host_block(L, i, P.arrays[i], "tinyllama_full_l16m", 3)
+        ref = [P.arrays[i].copy() for i in range(L.n_layers)]
+        hp, ohp = hparams_for("tinyllama_full_l16m", 3)
+        if path == "zero-copy":
+            lst.lst_zero_copy_step(L.handle, P.ptrs, hp, torch.cuda.current_stream().cuda_stream)
+            torch.cuda.synchronize()
+        else:
+            b0, b1 = _bufs(L)
+            lst.lst_stream_step(L.handle, P.ptrs, b0.data_ptr(), b1.data_ptr(), hp, 60_000)
+        assert P.guards_intact(), "a write outside a host block"
+        for i in range(L.n_layers):
+            oracle_step(L, ref[i], i, ohp)
+            assert np.array_equal(P.arrays[i], ref[i])
+    finally:
+        P.free()
+
+
 def test_stream_lora_many_small_blocks():
     _stream_vs_device(shapes.tinyllama_lora(), "L16F", "tinyllama_lora_l16f", 1, 1 << 16, steps=2)
 
