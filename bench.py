@@ -1,18 +1,21 @@
 """Benchmark: packed-state AdamW on GB300 (one JSON line on rank 0).
 
-Workload (default): the full TinyLlama-1.1B shape in the 16 B/param mixed
-layout (bf16 G | fp32 master | fp32 m | fp32 v | bf16 W), 24 blocks
-(embedding, 22 decoder layers, final norm + head), 1,100,048,384 parameters,
-17.6 GB of state; AdamW lr 1e-4, betas 0.9/0.999, eps 1e-8, wd 0.01.
-Inputs: the seeded synthetic generator (synth), step t starting at 1 with
-zero moments.
+Workload (default): the Llama-70B depth slice, 8 decoder layers (h 8,192, 64
+heads / 8 key-value heads, SwiGLU FFN 28,672; 855,654,400 parameters each,
+6,845,235,200 in all) in the 12 B/param layout (bf16 G | bf16 W | fp32 m |
+fp32 v), 82.1 GB of state; AdamW lr 1e-4, betas 0.9/0.999, eps 1e-8, wd 0.01.
+Inputs: the seeded synthetic generator (synth), step t starting at 1 with zero
+moments; the gradient of step t is drawn with seed + t.
 
   value     params/s of the device-resident step (lst_adamw_step, one
-            multi-block launch per step) with all state resident in HBM;
-            17.6 GB per launch, larger than L2, so no flush is needed.
-  e2e       params/s of the streamed step (lst_stream_step) over pinned
-            host blocks: every step copies the fields the update reads host
-            -> device and the fields it writes device -> host.
+            multi-block launch per step) with all 82 GB of state resident in
+            HBM (larger than the L2, so no flush is needed).
+  e2e       params/s of the streamed step (lst_stream_step) over pinned host
+            blocks for t = 1..3 from the initial state, a fresh gradient per
+            step: every step copies the fields the update reads host ->
+            device and the fields it writes device -> host.
+  e2e_before_heal  the same call on the pinned blocks as first allocated,
+            before the bench replaces slow pinned allocations.
   roofline  the fused update kernel against the measured HBM copy bandwidth.
   stream    pinned host-link bandwidth measured in the same run (H2D, D2H,
             both at once) and the streamed step against it.
@@ -20,8 +23,15 @@ zero moments.
             pinned host blocks directly (lst_zero_copy_step), against the
             same link roofline.
   stream_devgrad  the streamed step with the gradients already on the device
-            (lst_stream_step_devgrad): 12 B/param inbound instead of 14.
+            (lst_stream_step_devgrad): 10 B/param inbound instead of 12.
+  configs   the device-resident step (plain, per-block options, SGD form) on
+            the other workloads: one TinyLlama-1.1B layer, the full
+            TinyLlama-1.1B mixed layout, the TinyLlama LoRA adapters (L2
+            flushed) and LLaMA-7B.
   cpu_baseline  the oracle (plain C, all host cores) on a bounded sample.
+  parity    one block stepped by the product kernel and by the oracle, and
+            sampled elements of the streamed t = 1..3 result followed through
+            the three steps by the oracle.
 
 `--impl reference` times the oracle alone on the host, on the same workload.
 Under torchrun (N > 1) every rank runs its own replica of the workload on its
@@ -66,6 +76,13 @@ SGD_BYTES = {"L12": 6, "L16M": 12, "L16F": 12}
 SMALL_LAUNCH_BYTES = 256 << 20
 HP = dict(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
 HP_LORA = dict(lr=2e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+# The largest workload that fits one GPU: the Llama-70B depth slice (82.1 GB).
+DEFAULT_WORKLOAD = "llama70b_slice8_l12"
+# Workloads whose gradient is drawn afresh for every step t (seed + t), and
+# the streamed steps t = 1..n they are measured over from the initial state.
+FRESH_GRAD_STEPS = {"llama70b_slice8_l12": 3}
+# The other workloads, measured device-resident in the same run (configs).
+CONFIG_LEGS = ("tinyllama_layer_l12", "tinyllama_full_l16m", "tinyllama_lora_l16f", "llama7b_l12")
 
 
 # ---------------------------------------------------------------------------
@@ -149,11 +166,13 @@ def replica_seed(seed: int, rank: int) -> int:
 # clocks
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    """nvidia-smi clocks, utilisation and throttle reasons, sampled every
+    200 ms; the SM clock is summarised over the samples taken under load
+    (utilisation of at least 50 %, all samples if none is)."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -176,6 +195,10 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def snapshot(self):
+        """Summary of the samples so far (the sampler keeps running)."""
+        return self.summary(list(self.lines))
+
     def stop(self):
         if self.proc:
             self.proc.terminate()
@@ -185,22 +208,32 @@ class ClockSampler:
                 self.proc.kill()
         if self.thread:
             self.thread.join(timeout=5)
-        sm, mx, reasons = [], None, set()
+        return self.summary(self.lines)
+
+    @staticmethod
+    def summary(lines):
+        rows, mx = [], None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             p = [x.strip() for x in ln.split(",")]
             if len(p) < 9:
                 continue
             try:
-                sm.append(float(p[1]))
+                sm = float(p[1])
                 mx = float(p[2])
             except ValueError:
                 continue
-            for n, v in zip(names, p[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+            try:
+                util = float(p[9]) if len(p) > 9 else None
+            except ValueError:
+                util = None
+            rows.append((sm, util, {n for n, v in zip(names, p[5:9]) if v.lower() == "active"}))
+        loaded = [r for r in rows if r[1] is not None and r[1] >= 50.0] or rows
+        reasons = set()
+        for r in loaded:
+            reasons |= r[2]
+        return {"sm_mhz": statistics.median([r[0] for r in loaded]) if loaded else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded)}
 
 
 # ---------------------------------------------------------------------------
@@ -288,21 +321,53 @@ def anon_huge_page_bytes() -> int:
     return 0
 
 
+def grad_seed(workload: str, seed: int, t: int):
+    """Seed of step t's gradient: seed + t for the workloads that draw a fresh
+    gradient per step, None (the state's own seed) for the others."""
+    return seed + t if workload in FRESH_GRAD_STEPS else None
+
+
+def fill_blocks_parallel(jobs, workers: int = 8):
+    """Run fill jobs (callables) on a thread pool: the generator and numpy's
+    zero-fill release the GIL, so blocks fill in parallel."""
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=max(1, min(workers, len(jobs)))) as ex:
+        for f in [ex.submit(j) for j in jobs]:
+            f.result()
+
+
+def draw_state(L, arrs, workload: str, seed: int, first_block: int = 0):
+    """Every block of the state as at step t = 1 (zero moments), the
+    gradient of step 1; block i of L is block first_block + i of the model."""
+    import synth
+    fill_blocks_parallel([
+        (lambda i=i: synth.fill_block(L.numpy_views(i, arrs[i]), L.spans(i), first_block + i, workload, L.fmt,
+                                      t=1, seed=seed, g_seed=grad_seed(workload, seed, 1), threads=4))
+        for i in range(L.n_layers)])
+
+
+def redraw_gradients(L, arrs, workload: str, seed: int, t: int, first_block: int = 0):
+    """Step t's gradient (seed + t) into every block's G segment."""
+    import synth
+    gs = grad_seed(workload, seed, t)
+    fill_blocks_parallel([
+        (lambda i=i: synth.fill_field(L.numpy_views(i, arrs[i])["G"], "G", L.fmt, L.spans(i), first_block + i,
+                                      workload, t, gs, threads=4))
+        for i in range(L.n_layers)])
+
+
 def alloc_pinned_state(L, workload: str, seed: int, first_block: int = 0):
-    """Pinned host blocks drawn from the generator; block i of L is block
-    first_block + i of the model (a shard draws the model's own blocks)."""
+    """Pinned host blocks (lst_host_alloc) holding the state at t = 1."""
     import ctypes
     import numpy as np
-    import synth
     from optimizer_update_gb300 import lst
     ptrs, arrs = [], []
     for i in range(L.n_layers):
         n = L.block_bytes(i)
         p = lst.lst_host_alloc(n)
-        a = np.ctypeslib.as_array((ctypes.c_uint8 * n).from_address(p))
-        synth.fill_block(L.numpy_views(i, a), L.spans(i), first_block + i, workload, L.fmt, t=1, seed=seed)
         ptrs.append(p)
-        arrs.append(a)
+        arrs.append(np.ctypeslib.as_array((ctypes.c_uint8 * n).from_address(p)))
+    draw_state(L, arrs, workload, seed, first_block)
     return ptrs, arrs
 
 
@@ -335,6 +400,8 @@ def parity_sample(L, arrs, hp_kw, device, threads: int, t: int = 7):
     import oracle
     from optimizer_update_gb300 import Layout, lst
     i = max(range(L.n_layers), key=lambda k: (L.block(k)[1] if k else -1))  # the largest block but the first
+    if L.n_layers == 1:
+        i = 0
     Li = Layout([(name, (n,), 0) for (name, _off, n) in L.spans(i)], L.fmt)
     if Li.block_bytes(0) != L.block_bytes(i):
         return None
@@ -343,19 +410,28 @@ def parity_sample(L, arrs, hp_kw, device, threads: int, t: int = 7):
     lst.lst_adamw_step(Li.handle, [dev.data_ptr()], lst.adamw_hparams(step=t, **hp_kw),
                        torch.cuda.current_stream(device).cuda_stream)
     got = dev.cpu().numpy()
+    del dev
     oracle.step(L.fmt, Li.numpy_views(0, host), oracle.hparams(step=t, **hp_kw), threads=threads)
     gv, ev = Li.numpy_views(0, got), Li.numpy_views(0, host)
     out = {"block": i, "elements": int(Li.block(0)[1]), "step": t, "bit_exact": bool(np.array_equal(got, host))}
+    out.update(field_errors(L.fmt, gv, ev, Li.fields()))
+    return out
+
+
+def field_errors(fmt, got, exp, fields):
+    """Largest fp32 relative error, largest bf16 distance in ulps and the
+    number of NaN outputs over the written fields (G excluded)."""
+    import numpy as np
     rel, ulp, nans = 0.0, 0, 0
 
     def order(x):  # bf16 bit patterns in monotone integer order
         x = x.view(np.uint16).astype(np.int32)
         return np.where(x & 0x8000, 0x8000 - (x & 0x7FFF), x + 0x8000)
 
-    for f, dt in Li.fields().items():
+    for f, dt in fields.items():
         if f == "G":
             continue
-        a, b = gv[f], ev[f]
+        a, b = got[f], exp[f]
         if dt == "f32":
             an, bn = np.isnan(a), np.isnan(b)
         else:
@@ -372,85 +448,149 @@ def parity_sample(L, arrs, hp_kw, device, threads: int, t: int = 7):
             rel = max(rel, float(np.max(d)))
         else:
             ulp = max(ulp, int(np.max(np.abs(order(a) - order(b)))))
-    out["max_rel_err_fp32"] = rel
-    out["max_ulp_bf16"] = ulp
-    out["nan_outputs"] = nans
+    return {"max_rel_err_fp32": rel, "max_ulp_bf16": ulp, "nan_outputs": nans}
+
+
+def stream_samples(L, arrs, rng_seed: int = 11, n_random: int = 4096):
+    """Indices of every block (both ends, tensor boundaries, a random sample)
+    and the host state's values there: taken right after the streamed steps,
+    checked against the oracle later (parity_stream)."""
+    import numpy as np
+    rng = np.random.default_rng(rng_seed)
+    out = []
+    for i in range(L.n_layers):
+        p = L.padded(i)
+        idx = [np.arange(min(256, p)), np.arange(max(0, p - 256), p), rng.integers(0, p, n_random)]
+        for (_, off, n) in L.spans(i):
+            idx.append(np.array([e for e in (off, off + n - 1) if 0 <= e < p], dtype=np.int64))
+        idx = np.unique(np.concatenate(idx).astype(np.int64))
+        v = L.numpy_views(i, arrs[i])
+        out.append((idx, {f: v[f][idx].copy() for f in L.fields()}))
     return out
+
+
+def parity_stream(L, samples, workload: str, seed: int, hp_kw, steps: int, first_block: int = 0):
+    """The oracle follows the sampled elements from the generator's inputs at
+    t = 1 through steps t = 1..steps (step t's gradient drawn with
+    grad_seed(t)) and compares them with what the streamed steps left in the
+    host blocks: every byte, or the error figures."""
+    import numpy as np
+    import oracle
+    import synth
+    fields = L.fields()
+    n, exact, worst = 0, True, {"max_rel_err_fp32": 0.0, "max_ulp_bf16": 0, "nan_outputs": 0}
+    for i, (idx, got) in enumerate(samples):
+        blk = first_block + i
+        cur = {f: np.ascontiguousarray(synth.gather_block(f, L.fmt, L.spans(i), blk, workload, 1, idx, seed,
+                                                          grad_seed(workload, seed, 1))) for f in fields}
+        for t in range(1, steps + 1):
+            if t > 1:
+                cur["G"] = np.ascontiguousarray(synth.gather_block("G", L.fmt, L.spans(i), blk, workload, t, idx,
+                                                                   seed, grad_seed(workload, seed, t)))
+            oracle.step(L.fmt, cur, oracle.hparams(step=t, **hp_kw))
+        n += idx.size
+        for f in fields:
+            if f != "G" and not np.array_equal(got[f].view(np.uint8), cur[f].view(np.uint8)):
+                exact = False
+        e = field_errors(L.fmt, got, cur, fields)
+        worst = {k: max(worst[k], e[k]) if k != "nan_outputs" else worst[k] + e[k] for k in worst}
+    return dict({"steps": steps, "elements": n, "bit_exact": exact}, **worst)
 
 
 # ---------------------------------------------------------------------------
 def run_reference(args):
     """The oracle alone, on the host cores: each step a bounded sample of the
-    workload (whole blocks, as many as fit the per-step time budget)."""
+    workload. Geometry, inputs and arithmetic come from oracle/ and synth/
+    only; the product library is never loaded in this process."""
     import numpy as np
     import oracle
+    from oracle import layout as olayout
     import synth
     rank, _, world = dist_env()
     if rank != 0:
         return 0
-    L = build_layout(args.workload, args.max_blocks)
-    hp_kw = HP_LORA if L.fmt == "L16F" else HP
+    fmt = WORKLOADS[args.workload][1]
+    plan = olayout.plan(workload_specs(args.workload, args.max_blocks), fmt)
+    hp_kw = HP_LORA if fmt == "L16F" else HP
     threads = os.cpu_count() or 1
-    # state for the sample: blocks from the start of the model
-    arrs, blocks, budget_params = [], [], None
-    # size the sample so one step takes about --ref-step-s seconds
-    i = 0
-    # The sample is also bounded in memory (about 2 GiB of state), so that the
-    # reference run leaves the host's free memory much as it found it for the
-    # run measured after it.
-    state = 0
-    while i < L.n_layers and (state == 0 or state + L.block_bytes(i) <= (2 << 30)):
-        a = np.empty(L.block_bytes(i), np.uint8)
-        state += L.block_bytes(i)
-        synth.fill_block(L.numpy_views(i, a), L.spans(i), i, args.workload, L.fmt, t=1, seed=args.seed)
-        t0 = time.perf_counter()
-        oracle.step(L.fmt, L.numpy_views(i, a), oracle.hparams(step=1, **hp_kw), threads=threads)
-        dt = time.perf_counter() - t0
-        arrs.append(a)
-        blocks.append(i)
-        i += 1
-        total_est = dt * len(blocks)
-        if total_est >= args.ref_step_s:
+    # The sample: blocks from the start of the model, about 2 GiB of state at
+    # most (so the run leaves the host's memory much as it found it); a block
+    # larger than what is left contributes its first elements (the update is
+    # elementwise, so a prefix of every segment is a smaller block of the same
+    # kind). Stops early once a step would take --ref-step-s.
+    budget = args.ref_sample_bytes
+    sample, state, step_est = [], 0, 0.0
+    for b in plan.blocks:
+        if state >= budget or step_est >= args.ref_step_s:
             break
-    sample_params = sum(L.block(b)[1] for b in blocks)
+        per_elem = b.nbytes // max(1, b.padded)
+        if sample and budget - state < 2048 * per_elem:
+            break
+        n = b.padded if state + b.nbytes <= budget else max(2048, (budget - state) // per_elem // 2048 * 2048)
+        n = min(n, b.padded)
+        spans = [(name, off, max(0, min(cnt, n - off))) for (name, off, cnt) in b.spans if off < n]
+        fields = {f: np.zeros(n, olayout.field_dtype(fmt, f)) for f, _ in olayout.FORMATS[fmt]}
+        synth.fill_block(fields, spans, b.layer, args.workload, fmt, t=1, seed=args.seed,
+                         g_seed=grad_seed(args.workload, args.seed, 1))
+        t0 = time.perf_counter()
+        oracle.step(fmt, fields, oracle.hparams(step=1, **hp_kw), threads=threads)
+        step_est += time.perf_counter() - t0
+        sample.append((b.layer, n, fields, sum(c for (_, _, c) in spans)))
+        state += n * per_elem
+    sample_params = sum(s[3] for s in sample)
     for w in range(args.warmup):
-        for k, b in enumerate(blocks):
-            oracle.step(L.fmt, L.numpy_views(b, arrs[k]), oracle.hparams(step=2 + w, **hp_kw), threads=threads)
+        for (_, _, fields, _) in sample:
+            oracle.step(fmt, fields, oracle.hparams(step=2 + w, **hp_kw), threads=threads)
     t0 = time.perf_counter()
-    for s in range(args.steps):
-        for k, b in enumerate(blocks):
-            oracle.step(L.fmt, L.numpy_views(b, arrs[k]),
-                        oracle.hparams(step=2 + args.warmup + s, **hp_kw), threads=threads)
+    for k in range(args.steps):
+        for (_, _, fields, _) in sample:
+            oracle.step(fmt, fields, oracle.hparams(step=2 + args.warmup + k, **hp_kw), threads=threads)
     el = time.perf_counter() - t0
     value = sample_params * args.steps / el
-    sample = (f"blocks {blocks[0]}..{blocks[-1]} of {L.n_layers} ({sample_params} of {L.n_params} params) "
-              f"per step, oracle on {threads} threads")
+    last = sample[-1]
+    desc = (f"blocks {sample[0][0]}..{last[0]} of {len(plan.blocks)}"
+            + (f" (block {last[0]}: its first {last[1]} of {plan.blocks[last[0]].padded} elements)"
+               if last[1] < plan.blocks[last[0]].padded else "")
+            + f", {sample_params} of {plan.n_params} params per step, oracle on {threads} threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_for(L, args.workload, world, args.max_blocks),
-        "cpu_baseline": {"value": value, "unit": "params/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "config": config_for(fmt, plan.n_params, [b.nbytes for b in plan.blocks], args.workload, world,
+                             args.max_blocks),
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-def config_for(L, workload, world, max_blocks=0, shard=False, params_job=None):
+def l2_note(state_bytes: int) -> str:
+    return ("inputs larger than twice the L2 (no flush)" if state_bytes >= 2 * (132 << 20) else
+            "L2 flushed before every timed launch (a write of twice its size, then a read of another such buffer)")
+
+
+def config_for(fmt, n_params, block_bytes, workload, world, max_blocks=0, shard=False, params_job=None):
     desc = WORKLOADS[workload][2]
     if max_blocks > 0:
         desc += f", first {max_blocks} blocks only"
-    state = sum(L.block_bytes(i) for i in range(L.n_layers))
-    l2 = "inputs larger than twice the L2 (no flush)" if state >= 2 * (132 << 20) else \
-        "L2 flushed before every timed launch (a write of twice its size, then a read of another such buffer)"
+    state = sum(block_bytes)
     sharded = shard and world > 1
-    return {"workload": desc, "name": workload, "layout": L.fmt,
-            "params": int(params_job) if sharded and params_job else L.n_params,
-            "blocks": L.n_layers, "state_bytes": state, "l2": l2,
-            "parallelism": (f"blocks sharded x{world} (rank 0: {L.n_layers} blocks, {L.n_params} params)" if sharded
-                            else f"replicas x{world}"),
-            "hparams": HP_LORA if L.fmt == "L16F" else HP}
+    cfg = {"workload": desc, "name": workload, "layout": fmt,
+           "params": int(params_job) if sharded and params_job else int(n_params),
+           "blocks": len(block_bytes), "state_bytes": int(state), "l2": l2_note(state),
+           "parallelism": (f"blocks sharded x{world} (rank 0: {len(block_bytes)} blocks, {n_params} params)"
+                           if sharded else f"replicas x{world}"),
+           "hparams": HP_LORA if fmt == "L16F" else HP}
+    if workload in FRESH_GRAD_STEPS:
+        cfg["gradient"] = "drawn afresh for every step t with seed + t"
+        cfg["stream_steps"] = f"t = 1..{FRESH_GRAD_STEPS[workload]} from the initial state"
+    return cfg
+
+
+def layout_config(L, workload, world, max_blocks=0, shard=False, params_job=None):
+    return config_for(L.fmt, L.n_params, [L.block_bytes(i) for i in range(L.n_layers)], workload, world,
+                      max_blocks, shard, params_job)
 
 
 def block_h2d_rates(torch, arrs, dev):
@@ -550,6 +690,146 @@ def link_bandwidth(torch, host_ptr_arrs, dev_a, dev_b, nbytes: int, reps: int = 
             "d2h_concurrent_gbs": d2h_conc, "bytes": nbytes}
 
 
+def timed_launches(torch, stream, launch, steps, flush, flush_rd):
+    """Per-launch device times (s) of `steps` launches, CUDA events on the
+    launching stream around each, the L2 flushed before each when a flush
+    buffer is given (outside the event pair)."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for k in range(steps):
+        if flush is not None:
+            with torch.cuda.stream(stream):
+                flush.fill_(k & 0xFF)
+                flush_rd.sum()
+        starts[k].record(stream)
+        launch()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    return [starts[k].elapsed_time(ends[k]) / 1e3 for k in range(steps)]
+
+
+def l2_flush_buffers(torch, device, state_bytes: int):
+    """For a state under twice the L2: a buffer of twice the L2 to write (the
+    flush) and one to read (which writes the flush's dirty lines back), so a
+    timed launch starts cold and clean. (None, None) otherwise."""
+    l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or (132 << 20))
+    if state_bytes >= 2 * l2:
+        return None, None
+    return (torch.empty(2 * l2, dtype=torch.uint8, device=device),
+            torch.zeros(2 * l2 // 4, dtype=torch.int32, device=device))
+
+
+def device_leg(args, L, dptrs, hp_kw, stream, device, world, P_job, peak, t0_step: int = 1):
+    """The device-resident lst_adamw_step: warm-up, then args.steps timed
+    launches (one multi-block launch per step). Returns (result dict, next t,
+    per-launch times, flush buffers)."""
+    import torch
+    from optimizer_update_gb300 import lst
+    state_bytes = sum(L.block_bytes(i) for i in range(L.n_layers))
+    flush, flush_rd = l2_flush_buffers(torch, device, state_bytes)
+    ptr_arr = lst._ptr_array(dptrs)
+    hp = lst.adamw_hparams(step=t0_step, **hp_kw)
+    call = lst.lib().lst_adamw_step
+    t = [t0_step]
+
+    def launch():
+        hp.step = t[0]
+        st = call(L.handle, ptr_arr, ctypes.byref(hp), stream.cuda_stream)
+        if st != lst.LST_OK:
+            raise lst.LstError(st, lst.lst_last_error())
+        t[0] += 1
+
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize(device)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    per_launch = timed_launches(torch, stream, launch, args.steps, flush, flush_rd)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    t_dev = sum(per_launch)
+    t_dev_max = max_over_ranks(t_dev, device)
+    avg = t_dev / args.steps
+    alg_bytes = ALG_BYTES[L.fmt] * L.n_params
+    # the launch path picks the cross-run kernel below about twice the L2
+    kname = "lst_update_small_kernel" if alg_bytes < SMALL_LAUNCH_BYTES else "lst_update_kernel"
+    res = {"value": P_job * args.steps / t_dev_max, "t_dev_max": t_dev_max, "avg_launch": avg,
+           "achieved_gbs": alg_bytes / avg / 1e9, "frac_of_hbm_peak": alg_bytes / avg / 1e9 / peak,
+           "alg_bytes": alg_bytes, "kernel": kname, "per_launch": per_launch}
+    # state under twice the L2: also back to back without the flush (the
+    # launches then find part of the state in L2), beside the cold figure
+    if flush is not None:
+        wk = max(3, args.steps // 2)
+        wms = timed_launches(torch, stream, launch, wk, None, None)
+        res["back_to_back_l2_warm"] = {"median_launch_ms": 1e3 * statistics.median(wms), "launches": wk,
+                                       "algorithmic_gbs": alg_bytes / statistics.median(wms) / 1e9}
+    else:
+        res["back_to_back_l2_warm"] = None
+    return res, t[0], flush, flush_rd
+
+
+def device_blocks_from_generator(torch, L, workload, seed, device, first_block=0):
+    """Device blocks holding the state at t = 1, drawn block by block on the
+    host into one pinned staging buffer and copied over."""
+    import ctypes
+    import numpy as np
+    import synth
+    from optimizer_update_gb300 import lst
+    stage_p = lst.lst_host_alloc(max(1, L.max_block_bytes))
+    try:
+        stage = np.ctypeslib.as_array((ctypes.c_uint8 * max(1, L.max_block_bytes)).from_address(stage_p))
+        dev = []
+        for i in range(L.n_layers):
+            n = L.block_bytes(i)
+            synth.fill_block(L.numpy_views(i, stage[:n]), L.spans(i), first_block + i, workload, L.fmt, t=1,
+                             seed=seed, g_seed=grad_seed(workload, seed, 1))
+            d = torch.empty(n, dtype=torch.uint8, device=device)
+            d.copy_(torch.from_numpy(stage[:n]))
+            dev.append(d)
+        torch.cuda.synchronize(device)
+    finally:
+        lst.lst_host_free(stage_p)
+    return dev
+
+
+def configs_leg(args, device, world, seed, peak):
+    """The device-resident step (plain, per-block options, SGD form) on the
+    other workloads, each timed like the main device-resident leg."""
+    import torch
+    out = {}
+    for name in CONFIG_LEGS:
+        if name == args.workload:
+            continue
+        try:
+            L = build_layout(name)
+            hp_kw = HP_LORA if L.fmt == "L16F" else HP
+            dev = device_blocks_from_generator(torch, L, name, seed, device)
+            dptrs = [d.data_ptr() for d in dev]
+            stream = torch.cuda.Stream(device=device)
+            P_job = sum_over_ranks(L.n_params, device)
+            res, t, flush, flush_rd = device_leg(args, L, dptrs, hp_kw, stream, device, world, P_job, peak)
+            opt = time_options_leg(args, L, dptrs, hp_kw, stream, device, world, t, flush, flush_rd, peak)
+            sgd = time_sgd_leg(args, L, dptrs, hp_kw, stream, device, world, flush, flush_rd, peak)
+            state = sum(L.block_bytes(i) for i in range(L.n_layers))
+            out[name] = {"workload": WORKLOADS[name][2], "layout": L.fmt, "params": L.n_params,
+                         "blocks": L.n_layers, "state_bytes": state, "l2": l2_note(state),
+                         "value": res["value"], "unit": "params/s", "kernel": f"{res['kernel']}<{L.fmt}>",
+                         "achieved_gbs": res["achieved_gbs"], "frac_of_hbm_peak": res["frac_of_hbm_peak"],
+                         "avg_launch_ms": 1e3 * res["avg_launch"],
+                         "median_launch_ms": 1e3 * statistics.median(res["per_launch"]), "steps": args.steps,
+                         "back_to_back_l2_warm": res["back_to_back_l2_warm"],
+                         "options": {k: opt[k] for k in ("value", "frac_of_hbm_peak", "avg_launch_ms",
+                                                         "grad_sq_all_positive_finite")},
+                         "sgd": {k: sgd[k] for k in ("value", "frac_of_hbm_peak", "avg_launch_ms")}}
+            del dev, flush, flush_rd
+        except Exception as e:  # recorded in the line; the main result stands
+            out[name] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.synchronize(device)
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -568,8 +848,13 @@ def run_ours(args):
     P_job = sum_over_ranks(P, device)  # parameters all ranks update per step
     chunk = 1 << 24  # 16 Mi elements per sub-chunk (the library default)
     L.set_stream_chunk(chunk)
+    state_bytes = sum(L.block_bytes(i) for i in range(L.n_layers))
     ptrs, arrs = alloc_pinned_state(L, args.workload, seed, first_block)
     huge_bytes = anon_huge_page_bytes()  # the pinned blocks' share of huge pages
+    peak, peak_kind = measured_peaks()
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    clocks = ClockSampler(vis[local] if local < len(vis) else str(local))
+    clocks.start()
 
     # ---- device-resident leg -------------------------------------------------
     dev = []
@@ -579,100 +864,62 @@ def run_ours(args):
         dev.append(d)
     dptrs = [d.data_ptr() for d in dev]
     stream = torch.cuda.Stream(device=device)
-    t = 1
-    for _ in range(args.warmup):
-        lst.lst_adamw_step(L.handle, dptrs, lst.adamw_hparams(step=t, **hp_kw), stream.cuda_stream)
-        t += 1
-    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
-    clocks = ClockSampler(vis[local] if local < len(vis) else str(local))
-    clocks.start()
     time.sleep(0.3)
-    # State smaller than twice the L2: flush the L2 (write a buffer of twice its
-    # size) before every timed launch, outside the launch's event pair.
-    l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or (132 << 20))
-    state_bytes = sum(L.block_bytes(i) for i in range(L.n_layers))
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=device) if state_bytes < 2 * l2 else None
-    # the write leaves the L2 full of dirty lines; a read of a second buffer
-    # writes them back before the timed launch, which then starts cold and clean
-    flush_rd = torch.zeros(2 * l2 // 4, dtype=torch.int32, device=device) if flush is not None else None
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    torch.cuda.synchronize(device)
-    barrier(device)
-    torch.cuda.synchronize(device)
-    # arguments marshalled once: the host enqueues each launch with one C call
-    ptr_arr = lst._ptr_array(dptrs)
-    hp = lst.adamw_hparams(step=t, **hp_kw)
-    call = lst.lib().lst_adamw_step
-    for k in range(args.steps):
-        if flush is not None:
-            with torch.cuda.stream(stream):
-                flush.fill_(k & 0xFF)
-                flush_rd.sum()
-        starts[k].record(stream)
-        hp.step = t
-        st = call(L.handle, ptr_arr, ctypes.byref(hp), stream.cuda_stream)
-        if st != lst.LST_OK:
-            raise lst.LstError(st, lst.lst_last_error())
-        t += 1
-        ends[k].record(stream)
-    torch.cuda.synchronize(device)
-    barrier(device)
-    torch.cuda.synchronize(device)
-    clk = clocks.stop()
-    per_launch = [starts[k].elapsed_time(ends[k]) / 1e3 for k in range(args.steps)]
-    t_dev = sum(per_launch)
-    t_dev_max = max_over_ranks(t_dev, device)
-    value = P_job * args.steps / t_dev_max
-    avg_launch = t_dev / args.steps
-    alg_bytes = ALG_BYTES[L.fmt] * P
-    peak, peak_kind = measured_peaks()
-    achieved = alg_bytes / avg_launch / 1e9
-    # state under twice the L2: also back to back without the flush (the
-    # launches then find part of the state in L2), reported beside the cold
-    # figure and not as the value
-    warm_l2 = None
-    if flush is not None:
-        wk = max(3, args.steps // 2)
-        we = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(wk)]
-        for k in range(wk):
-            we[k][0].record(stream)
-            hp.step = t
-            st = call(L.handle, ptr_arr, ctypes.byref(hp), stream.cuda_stream)
-            if st != lst.LST_OK:
-                raise lst.LstError(st, lst.lst_last_error())
-            t += 1
-            we[k][1].record(stream)
-        torch.cuda.synchronize(device)
-        wms = [a.elapsed_time(b) for a, b in we]
-        warm_l2 = {"median_launch_ms": statistics.median(wms), "launches": wk,
-                   "algorithmic_gbs": alg_bytes / (statistics.median(wms) / 1e3) / 1e9}
-    # the launch path picks the cross-run kernel below about twice the L2
-    kname = "lst_update_small_kernel" if alg_bytes < SMALL_LAUNCH_BYTES else "lst_update_kernel"
+    res, t, flush, flush_rd = device_leg(args, L, dptrs, hp_kw, stream, device, world, P_job, peak)
+    clk = clocks.snapshot()
+    value, t_dev_max = res["value"], res["t_dev_max"]
+    avg_launch, per_launch, alg_bytes, kname = res["avg_launch"], res["per_launch"], res["alg_bytes"], res["kernel"]
+    achieved = res["achieved_gbs"]
     traffic = kernel_traffic(kname, L.fmt, P)
     # ---- per-block options leg: lst_adamw_step_ex with a step counter per
     # block (staggered, as after progressive locking) and every block's
     # sum of g^2 returned by the same pass ---------------------------------------
     options = time_options_leg(args, L, dptrs, hp_kw, stream, device, world, t, flush, flush_rd, peak)
     sgd = time_sgd_leg(args, L, dptrs, hp_kw, stream, device, world, flush, flush_rd, peak)
-    del dev
+    del dev, flush, flush_rd
     torch.cuda.empty_cache()
 
     # ---- host link, measured in this run -------------------------------------
     buf0 = torch.empty(L.max_block_bytes, dtype=torch.uint8, device=device)
     buf1 = torch.empty(L.max_block_bytes, dtype=torch.uint8, device=device)
     big = [i for i in range(L.n_layers) if L.block_bytes(i) >= min(1 << 30, L.max_block_bytes)]
-    a0 = arrs[big[0]] if big else arrs[0]
-    a1 = arrs[big[-1]] if len(big) > 1 else arrs[-1]
-    nb = min(a0.size, a1.size, buf0.numel(), 1 << 30)
+    nb = min(arrs[big[0] if big else 0].size, arrs[big[-1] if len(big) > 1 else -1].size, buf0.numel(), 1 << 30)
+
+    def probe_pair():
+        return (arrs[big[0]] if big else arrs[0]), (arrs[big[-1]] if len(big) > 1 else arrs[-1])
+
+    h2d_b = sum(L.transfer(i)[1] for i in range(L.n_layers))
+    d2h_b = sum(L.transfer(i)[3] for i in range(L.n_layers))
+    n_stream = FRESH_GRAD_STEPS.get(args.workload, max(1, min(args.steps, args.e2e_steps)))
+
+    def stream_call(tt):
+        lst.lst_stream_step(L.handle, ptrs, buf0.data_ptr(), buf1.data_ptr(), lst.adamw_hparams(step=tt, **hp_kw),
+                            600_000)
+
+    # ---- the streamed step as a caller gets it: the pinned blocks as first
+    # allocated, before the health check below replaces slow allocations -------
+    link_before = link_bandwidth(torch, list(probe_pair()), buf0, buf1, nb)
+    pre = []
+    for k in range(3):
+        t0w = time.perf_counter()
+        stream_call(t)
+        t += 1
+        pre.append(time.perf_counter() - t0w)
+    rates_before = block_h2d_rates(torch, arrs, buf0)
+    roof_before = max(h2d_b / (link_before["h2d_concurrent_gbs"] * 1e9),
+                      d2h_b / (link_before["d2h_concurrent_gbs"] * 1e9))
+    e2e_before_heal = {"value": P_job / statistics.median(pre), "unit": "params/s", "call": "lst_stream_step",
+                       "step_ms": [1e3 * x for x in pre], "median_step_ms": 1e3 * statistics.median(pre),
+                       "frac_of_link_roofline": roof_before / statistics.median(pre),
+                       "note": "first three calls on the pinned blocks as allocated (lst_host_alloc), "
+                               "before slow allocations are replaced",
+                       "block_h2d_gbs_min": min(rates_before),
+                       "slow_blocks": sum(1 for r in rates_before if r < 0.5 * max(rates_before))}
     slow_before_heal, healed, retired = heal_pinned_state(torch, L, ptrs, arrs, buf0)
-    a0 = arrs[big[0]] if big else arrs[0]
-    a1 = arrs[big[-1]] if len(big) > 1 else arrs[-1]
+    a0, a1 = probe_pair()
     link = link_bandwidth(torch, [a0, a1], buf0, buf1, nb)
 
     # ---- streamed leg (the public end-to-end call) ------------------------------
-    h2d_b = sum(L.transfer(i)[1] for i in range(L.n_layers))
-    d2h_b = sum(L.transfer(i)[3] for i in range(L.n_layers))
     # On the shared hosts here, host-link throughput also varies from moment
     # to moment (besides the slow allocations the health check above
     # replaces). Untimed warm-up steps until two in a row agree within 5 % (at
@@ -690,38 +937,52 @@ def run_ours(args):
                 return n_warm
             prev = dt
 
-    stream_warm = warm(lambda tt: lst.lst_stream_step(L.handle, ptrs, buf0.data_ptr(), buf1.data_ptr(),
-                                                      lst.adamw_hparams(step=tt, **hp_kw), 600_000))
-    # every block's own host-to-device rate, after the warm-up and right
-    # before the timed steps (a slow pinned allocation holds up the pipeline)
+    stream_warm = warm(stream_call)
+    # The timed steps start from the initial state: t = 1 with zero moments
+    # and step 1's gradient, each later step's gradient drawn before the step
+    # (outside the timed region, standing in for the backward pass).
+    if args.workload in FRESH_GRAD_STEPS:
+        draw_state(L, arrs, args.workload, seed, first_block)
+        t_first = 1
+    else:
+        t_first = t
+    # every block's own host-to-device rate, right before the timed steps
+    # (a slow pinned allocation holds up the pipeline)
     block_rates = block_h2d_rates(torch, arrs, buf0)
-    e_steps = max(1, min(args.steps, args.e2e_steps))
-    torch.cuda.synchronize(device)
-    barrier(device)
-    torch.cuda.synchronize(device)
-    t0 = time.perf_counter()
-    for _ in range(e_steps):
-        lst.lst_stream_step(L.handle, ptrs, buf0.data_ptr(), buf1.data_ptr(),
-                            lst.adamw_hparams(step=t, **hp_kw), 600_000)
-        t += 1
-    torch.cuda.synchronize(device)
-    t_e2e = time.perf_counter() - t0
+    step_times = []
+    for k in range(n_stream):
+        tt = t_first + k
+        if args.workload in FRESH_GRAD_STEPS and k > 0:
+            redraw_gradients(L, arrs, args.workload, seed, tt, first_block)
+        torch.cuda.synchronize(device)
+        barrier(device)
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        stream_call(tt)
+        torch.cuda.synchronize(device)
+        step_times.append(time.perf_counter() - t0)
+    t = max(t, t_first + n_stream)
+    samples = stream_samples(L, arrs) if (rank == 0 and args.workload in FRESH_GRAD_STEPS) else None
+    t_e2e = sum(step_times)
     t_e2e_max = max_over_ranks(t_e2e, device)
-    e2e_value = P_job * e_steps / t_e2e_max
+    e2e_value = P_job * n_stream / t_e2e_max
     chunks = sum((L.padded(i) + chunk - 1) // chunk for i in range(L.n_layers))
     roof_t = max(h2d_b / (link["h2d_concurrent_gbs"] * 1e9), d2h_b / (link["d2h_concurrent_gbs"] * 1e9))
     # the same bytes with the two directions one after the other (each at its
     # measured bandwidth alone): what the three-stream overlap saves
     serial_t = h2d_b / (link["h2d_gbs"] * 1e9) + d2h_b / (link["d2h_gbs"] * 1e9)
-    stream_info = dict(link, step_ms=1e3 * t_e2e / e_steps, serial_copies_ms=1e3 * serial_t,
-                       achieved_h2d_gbs=h2d_b * e_steps / t_e2e / 1e9,
-                       achieved_d2h_gbs=d2h_b * e_steps / t_e2e / 1e9,
-                       roofline_ms=1e3 * roof_t, frac_of_link_roofline=roof_t / (t_e2e / e_steps),
+    stream_info = dict(link, step_ms=1e3 * t_e2e / n_stream, step_ms_each=[1e3 * x for x in step_times],
+                       steps=n_stream, t_first=t_first, serial_copies_ms=1e3 * serial_t,
+                       achieved_h2d_gbs=h2d_b * n_stream / t_e2e / 1e9,
+                       achieved_d2h_gbs=d2h_b * n_stream / t_e2e / 1e9,
+                       roofline_ms=1e3 * roof_t, frac_of_link_roofline=roof_t / (t_e2e / n_stream),
                        chunk_elems=chunk, warmup_steps=stream_warm,
                        host_huge_page_bytes=huge_bytes, host_state_bytes=state_bytes,
                        block_h2d_gbs_min=min(block_rates), block_h2d_gbs_median=statistics.median(block_rates),
                        slow_blocks=sum(1 for r in block_rates if r < 0.5 * link["h2d_gbs"]),
-                       slow_blocks_before_heal=slow_before_heal, healed_blocks=healed)
+                       slow_blocks_before_heal=slow_before_heal, healed_blocks=healed,
+                       link_before_heal={k: link_before[k] for k in ("h2d_gbs", "d2h_gbs", "h2d_concurrent_gbs",
+                                                                     "d2h_concurrent_gbs")})
 
     # ---- streamed leg with device-resident gradients: only the state crosses
     # the link inbound (the gradients stand for what a backward pass leaves on
@@ -737,6 +998,7 @@ def run_ours(args):
     devgrad_warm = warm(lambda tt: lst.lst_stream_step_devgrad(L.handle, ptrs, gptrs, buf0.data_ptr(),
                                                                buf1.data_ptr(), lst.adamw_hparams(step=tt, **hp_kw),
                                                                None, 600_000))
+    e_steps = n_stream
     barrier(device)
     t0 = time.perf_counter()
     for _ in range(e_steps):
@@ -777,6 +1039,8 @@ def run_ours(args):
     store = None
     if args.store_dir:
         store = run_store_leg(args, L, ptrs, buf0, buf1, hp_kw, device, world, rank)
+    del buf0, buf1
+    torch.cuda.empty_cache()
 
     # ---- CPU baseline: the oracle on the host cores, bounded sample ------------
     cpu, parity = None, None
@@ -786,9 +1050,16 @@ def run_ours(args):
         cpu = {"value": rate, "unit": "params/s", "cores": threads, "kind": "oracle",
                "sample": f"{nblocks} block updates ({done} params) of this workload's state in {el:.1f} s"}
         parity = parity_sample(L, arrs, hp_kw, device, threads)
+        if samples is not None and parity is not None:
+            parity["stream"] = parity_stream(L, samples, args.workload, seed, hp_kw, n_stream, first_block)
 
     for p in ptrs + retired:
         lst.lst_host_free(p)
+    arrs = []
+
+    # ---- the other workloads, device-resident --------------------------------
+    configs = configs_leg(args, device, world, seed, peak) if not args.no_configs else None
+    clk_all = clocks.stop()
 
     if rank == 0:
         line = {
@@ -796,25 +1067,28 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": 1e3 * t_dev_max / args.steps, "higher_is_better": True,
             "scaling": "strong" if (args.shard and world > 1) else "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": config_for(L, args.workload, world, args.max_blocks, args.shard, P_job),
+            "config": layout_config(L, args.workload, world, args.max_blocks, args.shard, P_job),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": f"{kname}<{L.fmt}>", "alg_bytes_per_launch": alg_bytes,
                          "avg_launch_ms": 1e3 * avg_launch, "median_launch_ms": 1e3 * statistics.median(per_launch),
                          "min_launch_ms": 1e3 * min(per_launch), "peak_source": f"{peak_kind} hbm_gbs",
-                         "back_to_back_l2_warm": warm_l2},
+                         "back_to_back_l2_warm": res["back_to_back_l2_warm"]},
             "e2e": {"value": e2e_value, "unit": "params/s", "h2d_bytes_per_step": h2d_b,
-                    "d2h_bytes_per_step": d2h_b, "steps": e_steps, "call": "lst_stream_step",
-                    "gpu_launches": e_steps * chunks},
+                    "d2h_bytes_per_step": d2h_b, "steps": n_stream, "call": "lst_stream_step",
+                    "gpu_launches": n_stream * chunks},
+            "e2e_before_heal": e2e_before_heal,
             "options": options,
             "sgd": sgd,
             "stream": stream_info,
             "zero_copy": zero_copy,
             "stream_devgrad": stream_devgrad,
             **({"store": store} if store is not None else {}),
+            "configs": configs,
             "cpu_baseline": cpu,
             "parity": parity,
             "clocks": clk,
+            "clocks_whole_run": clk_all,
             "gpu_launches": args.steps,
         }
         print(json.dumps(line), flush=True)
@@ -995,12 +1269,16 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="tinyllama_full_l16m")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=0x5EED)
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)
+    ap.add_argument("--ref-sample-bytes", type=int, default=2 << 30,
+                    help="state the reference arm's sample holds at most")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the device-resident legs on the other workloads (configs object)")
     ap.add_argument("--shard", action="store_true",
                     help="with N > 1: each rank updates a contiguous range of the model's blocks (strong scaling) "
                          "instead of a replica of the whole model (weak scaling, the default)")

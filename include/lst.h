@@ -260,14 +260,16 @@ LST_API lst_status lst_adamw_step_ex(const lst_layout* layout, void* const* dev_
    it is running.
    The scratch is one static device array of lst_workspace_bytes() bytes
    (1 MiB + 256 bytes). Every GPU that loads the library's device code holds
-   it until the process exits. It holds the partial sums of one launch, so
-   when grad_sq is given at most 128 blocks may be updated per call (blocks
-   marked in skip do not count); more gives LST_ERR_INVALID_ARG and touches
-   nothing. Without grad_sq no scratch is used and there is no limit.
+   it until the process exits. It holds the partial sums of one launch (128
+   blocks); a step over more blocks runs as several launches in order on the
+   one stream, which reuse the array one after the other, so there is no limit
+   on the number of blocks. Without grad_sq no scratch is used.
    The first call on a device that passes grad_sq looks up the array's device
    address (cudaGetSymbolAddress) with that device current; make that first
-   call before any stream capture. The call allocates nothing: no cudaMalloc,
-   no cudaFree, no allocating library routine.
+   call before any stream capture. The address is kept for the process's
+   lifetime: the call assumes the runtime's primary context on each device and
+   no cudaDeviceReset after that first call. The call allocates nothing: no
+   cudaMalloc, no cudaFree, no allocating library routine.
    All calls share the one array, which keeps the last call's contents;
    nothing in it needs to start at any value. Calls whose
    work overlaps on the GPU (streams with no ordering between them) race on

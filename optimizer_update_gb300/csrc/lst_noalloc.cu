@@ -27,7 +27,10 @@ static std::mutex g_noalloc_mu;
 // Device address of the array on the current device. The name
 // g_noalloc_workspace is only a host-side handle: passing it to a kernel
 // would hand the device a host address. So, once per device and with that
-// device current, ask the runtime for the array's device address.
+// device current, ask the runtime for the array's device address. The address
+// is kept for the life of the process: it belongs to the device's primary
+// context (the one the CUDA runtime uses), and stays valid as long as that
+// context does, i.e. until cudaDeviceReset.
 static cudaError_t noalloc_workspace(void** out) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -60,16 +63,10 @@ extern "C" lst_status lst_adamw_step_ex_noalloc(const lst_layout* L, void* const
                 "lst_adamw_step_ex_noalloc: hyperparameters outside their domain (step >= 1, 0 <= beta < 1, finite)");
   void* ws = nullptr;
   if (grad_sq) {
-    // The array holds the partial sums of one launch: at most 128 blocks.
-    const int64_t n = (int64_t)L->blocks.size();
-    int64_t active = 0;
-    for (int64_t i = 0; i < n; ++i)
-      if (!(skip && skip[i])) ++active;
-    if (active > kMaxRunsPerLaunch)
-      return fail(LST_ERR_INVALID_ARG,
-                  "lst_adamw_step_ex_noalloc: %lld blocks to update with grad_sq; the built-in scratch holds "
-                  "the sums of at most %d blocks per call",
-                  (long long)active, kMaxRunsPerLaunch);
+    // The array holds the partial sums of one launch (up to 128 blocks). A
+    // step over more blocks runs as several launches on the one stream, each
+    // update launch after the first starting only once the previous launch's
+    // reduce has finished reading the array, so any number of blocks share it.
     cudaError_t err = noalloc_workspace(&ws);
     if (err != cudaSuccess) return cuda_fail(err, "lst_adamw_step_ex_noalloc: scratch address");
   }

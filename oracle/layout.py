@@ -120,3 +120,21 @@ def plan(specs: Sequence[Tuple[str, Sequence[int], int]], fmt: str) -> Layout:
         last_out = b.segments[OUTPUTS[fmt][-1]]
         b.d2h = (first_out, last_out[0] + last_out[1] - first_out)
     return Layout(fmt, blocks, tensor_block, tensor_off)
+
+
+def field_dtype(fmt: str, fieldname: str) -> str:
+    """numpy dtype name of a field's elements: bf16 fields as uint16 bit
+    patterns, fp32 fields as float32."""
+    return "uint16" if dict(FORMATS[fmt])[fieldname] == 2 else "float32"
+
+
+def views(fmt: str, block: Block, buf):
+    """Typed numpy views of one block's field segments over the block's bytes
+    (a uint8 array of block.nbytes bytes): field -> 1-D array of block.padded
+    elements."""
+    import numpy as np
+    out = {}
+    for fname, _es in FORMATS[fmt]:
+        off, size = block.segments[fname]
+        out[fname] = buf[off:off + size].view(np.dtype(field_dtype(fmt, fname)))
+    return out

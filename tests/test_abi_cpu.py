@@ -3,6 +3,7 @@ the oracle's calculator), argument validation that happens before any CUDA
 call, status strings."""
 
 import ctypes
+import json
 import os
 import re
 
@@ -204,7 +205,7 @@ def test_bench_runs_the_oracle_only_in_its_baseline_and_reference_legs():
                     importers.add(fn.name)
                 if isinstance(node, ast.ImportFrom) and (node.module or "").split(".")[0] == "oracle":
                     importers.add(fn.name)
-    assert importers == {"cpu_oracle_rate", "parity_sample", "run_reference"}
+    assert importers == {"cpu_oracle_rate", "parity_sample", "parity_stream", "run_reference"}
     # no module-level import of the oracle
     for node in tree.body:
         if isinstance(node, (ast.Import, ast.ImportFrom)):
@@ -212,8 +213,34 @@ def test_bench_runs_the_oracle_only_in_its_baseline_and_reference_legs():
             assert not any(n.split(".")[0] == "oracle" for n in names)
     # the baseline helpers are called only under the CPU-baseline condition
     src = open(os.path.join(ROOT, "bench.py")).read()
-    for helper in ("cpu_oracle_rate(", "parity_sample("):
+    for helper in ("cpu_oracle_rate(", "parity_sample(", "parity_stream("):
         calls = [i for i in range(len(src)) if src.startswith(helper, i) and not src[:i].endswith("def ")]
         assert len(calls) == 1, helper
         guard = src.rfind("if rank == 0 and world == 1 and not args.no_cpu_baseline:", 0, calls[0])
-        assert guard != -1 and calls[0] - guard < 600, helper
+        assert guard != -1 and calls[0] - guard < 800, helper
+
+
+def test_bench_reference_arm_uses_only_the_oracle_and_the_generator():
+    """bench.py --impl reference builds its geometry, inputs and steps from
+    oracle/ and synth/ alone: the product library is never imported or
+    loaded in that process (a 4 MiB sample of the Llama-70B slice's first
+    block, one timed step)."""
+    import subprocess
+    import sys
+    code = (
+        "import sys, json\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import bench\n"
+        "rc = bench.main(['--impl', 'reference', '--steps', '1', '--warmup', '3', '--ref-step-s', '0.01',"
+        " '--ref-sample-bytes', str(4 << 20)])\n"
+        "maps = open('/proc/self/maps').read()\n"
+        "print('LOADED', 'liblst.so' in maps, 'optimizer_update_gb300' in sys.modules)\n"
+        "sys.exit(rc)\n")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    lines = out.stdout.strip().splitlines()
+    line = json.loads([x for x in lines if x.startswith("{")][0])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["config"]["name"] == "llama70b_slice8_l12"
+    assert "first" in line["cpu_baseline"]["sample"]
+    assert lines[-1] == "LOADED False False"

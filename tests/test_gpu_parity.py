@@ -159,7 +159,7 @@ def test_padding_stays_zero():
 
 # ---- full sizes, sampled (the launch configuration the bench times: one
 # multi-block launch over every block of the model)
-def _full_size_sampled(specs, fmt, workload, t, seed_rng):
+def _full_size_sampled(specs, fmt, workload, t, seed_rng, sgd=False):
     L = Layout(specs, fmt)
     host = np.empty(L.max_block_bytes, np.uint8)
     blocks = []
@@ -170,17 +170,25 @@ def _full_size_sampled(specs, fmt, workload, t, seed_rng):
         b.copy_(torch.from_numpy(host[:n]))
         blocks.append(b)
     hp, ohp = hparams_for(workload, t)
-    lst.lst_adamw_step(L.handle, [b.data_ptr() for b in blocks], hp, _stream())
+    if sgd:
+        lst.lst_sgd_step(L.handle, [b.data_ptr() for b in blocks], hp.lr, _stream())
+    else:
+        lst.lst_adamw_step(L.handle, [b.data_ptr() for b in blocks], hp, _stream())
     torch.cuda.synchronize()
     rng = np.random.default_rng(seed_rng)
     checked = 0
     for i in range(L.n_layers):
         idx = sample_indices(L.padded(i), L.spans(i), rng)
         inp = gathered_inputs(L, i, workload, t, idx)
-        oracle.step(fmt, inp, ohp)
+        before = {f: a.copy() for f, a in inp.items()}
+        oracle.step(fmt, inp, ohp, sgd=sgd)
         got = gather_device(L.torch_views(i, blocks[i]), idx)
-        s = compare(fmt, got, inp)
+        fields = (("MASTER", "W") if fmt == "L16M" else ("W",)) if sgd else None
+        s = compare(fmt, got, inp, fields)
         _assert_bit_exact([s])
+        if sgd:  # the moments are neither read nor written
+            for f in ("M", "V"):
+                assert np.array_equal(got[f].view(np.uint32), before[f].view(np.uint32)), f
         checked += idx.size
     del blocks
     return checked
@@ -194,6 +202,26 @@ def test_tinyllama_full_l16m_sampled():
 @pytest.mark.slow
 def test_llama7b_l12_sampled():
     assert _full_size_sampled(shapes.llama7b(), "L12", "llama7b_l12", 10, 2) > 100_000
+
+
+# ---- the SGD form through the large-launch kernels (the launches the bench
+# times): three TinyLlama-1.1B layers per layout in one launch, every element
+# of every block against the oracle, bit for bit (one and two waves of CTAs)
+@pytest.mark.parametrize("fmt", ["L12", "L16M", "L16F"])
+def test_sgd_three_layers_large_launch_full(fmt):
+    specs = [(n, sh, l - 1) for (n, sh, l) in shapes.tinyllama_full() if l in (1, 2, 3)]
+    L, stats = _run_full(specs, fmt, "tinyllama_full_l16m" if fmt == "L16M" else "sgd_three_layers", 4, sgd=True)
+    alg = 22 if fmt == "L12" else 28
+    assert L.n_params * alg > (256 << 20)  # above the small-launch threshold
+    _assert_bit_exact(stats)
+
+
+# ... and over the whole TinyLlama-1.1B state (more than 8 GB per launch: the
+# 16 B layouts' three-wave grid), sampled
+@pytest.mark.slow
+@pytest.mark.parametrize("fmt", ["L16M", "L16F"])
+def test_sgd_tinyllama_full_sampled(fmt):
+    assert _full_size_sampled(shapes.tinyllama_full(), fmt, "tinyllama_full_l16m", 6, 3, sgd=True) > 100_000
 
 
 @pytest.mark.parametrize("fmt", ["L12", "L16M", "L16F"])
