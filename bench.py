@@ -922,22 +922,9 @@ def run_ours(args):
     # ---- streamed leg (the public end-to-end call) ------------------------------
     # On the shared hosts here, host-link throughput also varies from moment
     # to moment (besides the slow allocations the health check above
-    # replaces). Untimed warm-up steps until two in a row agree within 5 % (at
-    # least 3, at most 12); the link is measured again after the streamed legs.
-    def warm(call):
-        nonlocal t
-        prev, n_warm = None, 0
-        while True:
-            t0w = time.perf_counter()
-            call(t)
-            t += 1
-            n_warm += 1
-            dt = time.perf_counter() - t0w
-            if (n_warm >= 3 and prev is not None and abs(dt - prev) <= 0.05 * prev) or n_warm >= 12:
-                return n_warm
-            prev = dt
-
-    stream_warm = warm(stream_call)
+    # replaces), so the streamed legs warm up until two steps agree; the link
+    # is measured again after the streamed legs.
+    stream_warm, t = warm_until_stable(stream_call, t)
     # The timed steps start from the initial state: t = 1 with zero moments
     # and step 1's gradient, each later step's gradient drawn before the step
     # (outside the timed region, standing in for the backward pass).
@@ -984,41 +971,21 @@ def run_ours(args):
                        link_before_heal={k: link_before[k] for k in ("h2d_gbs", "d2h_gbs", "h2d_concurrent_gbs",
                                                                      "d2h_concurrent_gbs")})
 
-    # ---- streamed leg with device-resident gradients: only the state crosses
-    # the link inbound (the gradients stand for what a backward pass leaves on
-    # the device; producing them is not part of the timed step) ---------------
-    grads = []
-    for i in range(L.n_layers):
-        goff, gbytes = L.segment(i, "G")
-        g = torch.empty(gbytes, dtype=torch.uint8, device=device)
-        g.copy_(torch.from_numpy(arrs[i][goff:goff + gbytes]))
-        grads.append(g)
-    gptrs = [g.data_ptr() for g in grads]
-    dg_h2d = sum(L.transfer(i)[1] - L.segment(i, "G")[1] for i in range(L.n_layers))
-    devgrad_warm = warm(lambda tt: lst.lst_stream_step_devgrad(L.handle, ptrs, gptrs, buf0.data_ptr(),
-                                                               buf1.data_ptr(), lst.adamw_hparams(step=tt, **hp_kw),
-                                                               None, 600_000))
-    e_steps = n_stream
-    barrier(device)
-    t0 = time.perf_counter()
-    for _ in range(e_steps):
-        lst.lst_stream_step_devgrad(L.handle, ptrs, gptrs, buf0.data_ptr(), buf1.data_ptr(),
-                                    lst.adamw_hparams(step=t, **hp_kw), None, 600_000)
-        t += 1
-    t_dg = max_over_ranks(time.perf_counter() - t0, device)
-    roof_dg = max(dg_h2d / (link["h2d_concurrent_gbs"] * 1e9), d2h_b / (link["d2h_concurrent_gbs"] * 1e9))
-    stream_devgrad = {"value": P_job * e_steps / t_dg, "unit": "params/s", "call": "lst_stream_step_devgrad",
-                      "step_ms": 1e3 * t_dg / e_steps, "h2d_bytes_per_step": dg_h2d, "d2h_bytes_per_step": d2h_b,
-                      "roofline_ms": 1e3 * roof_dg, "frac_of_link_roofline": roof_dg / (t_dg / e_steps),
-                      "steps": e_steps, "warmup_steps": devgrad_warm}
-    del grads
+    # ---- streamed leg with the gradients produced on the device by a
+    # backward stand-in (the generator's GPU twin), block by block last to
+    # first, each block released by its Backward-Done event: only the state
+    # crosses the link inbound, and the step overlaps the production ---------
+    stream_devgrad = devgrad_leg(args, L, ptrs, buf0, buf1, hp_kw, device, P_job, link, d2h_b, seed, first_block,
+                                 t)
+    t = stream_devgrad.pop("next_t")
 
     # ---- zero-copy leg: the update kernel directly on the pinned host blocks ----
     zstream = torch.cuda.Stream(device=device)
     def zc_call(tt):
         lst.lst_zero_copy_step(L.handle, ptrs, lst.adamw_hparams(step=tt, **hp_kw), zstream.cuda_stream)
         torch.cuda.synchronize(device)
-    zc_warm = warm(zc_call)
+    zc_warm, t = warm_until_stable(zc_call, t)
+    e_steps = n_stream
     barrier(device)
     zs, ze = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     zs.record(zstream)
@@ -1096,6 +1063,132 @@ def run_ours(args):
     if dist.is_available() and dist.is_initialized():
         dist.destroy_process_group()
     return 0
+
+
+def warm_until_stable(call, t: int, lo: int = 3, hi: int = 12, tol: float = 0.05):
+    """Untimed calls call(t), call(t + 1), ... until two in a row take times
+    within `tol` of each other (at least `lo` calls, at most `hi`). Returns
+    (calls made, the next step counter)."""
+    prev, n = None, 0
+    while True:
+        t0 = time.perf_counter()
+        call(t)
+        t += 1
+        n += 1
+        dt = time.perf_counter() - t0
+        if (n >= lo and prev is not None and abs(dt - prev) <= tol * prev) or n >= hi:
+            return n, t
+        prev = dt
+
+
+def devgrad_leg(args, L, ptrs, buf0, buf1, hp_kw, device, P_job, link, d2h_b, seed, first_block, t):
+    """lst_stream_step_devgrad_events fed by a gradient producer on the
+    device (synth.device_fill_field: the generator's values, written block by
+    block in backward order, n-1 .. 0, on its own stream, an event recorded
+    after each block). The timed region of a step holds the production and
+    the streamed step: from before the producer is enqueued until the call
+    returns. Step t's gradient is drawn with grad_seed(t). The roofline is
+    max(producer alone, the link time of the bytes moved). A second
+    measurement slows the producer (extra hash rounds per element, calibrated
+    to about 0.8 of the link time) to show the two overlapping: the step then
+    takes about the larger of the two, not their sum."""
+    import torch
+    import synth
+    from optimizer_update_gb300 import lst
+    n = L.n_layers
+    order = list(reversed(range(n)))
+    grads = [torch.empty(L.segment(i, "G")[1], dtype=torch.uint8, device=device) for i in range(n)]
+    gptrs = [g.data_ptr() for g in grads]
+    producer = torch.cuda.Stream(device=device)
+    dg_h2d = sum(L.transfer(i)[1] - L.segment(i, "G")[1] for i in range(n))
+    roof_link = max(dg_h2d / (link["h2d_concurrent_gbs"] * 1e9), d2h_b / (link["d2h_concurrent_gbs"] * 1e9))
+
+    def produce(tt, passes, events=None):
+        gs = grad_seed(args.workload, seed, tt)
+        for i in order:
+            synth.device_fill_field(gptrs[i], "G", L.fmt, L.spans(i), L.padded(i), first_block + i, args.workload,
+                                    tt, seed if gs is None else gs, producer.cuda_stream, passes)
+            if events is not None:
+                events[i].record(producer)
+
+    def producer_alone(tt, passes, reps=2):
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(device)
+            e0.record(producer)
+            produce(tt, passes)
+            e1.record(producer)
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1) / 1e3)
+        return best
+
+    def overlapped(tt, passes):
+        """One step: enqueue the producer (async), then the synchronous
+        streamed step; wall time of both."""
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        events = [torch.cuda.Event() for _ in range(n)]
+        produce(tt, passes, events)
+        lst.lst_stream_step_devgrad_events(L.handle, ptrs, gptrs, [e.cuda_event for e in events], order,
+                                           buf0.data_ptr(), buf1.data_ptr(), lst.adamw_hparams(step=tt, **hp_kw),
+                                           None, 600_000)
+        torch.cuda.synchronize(device)
+        return time.perf_counter() - t0
+
+    def serial(tt, passes):
+        """The same work without overlap: produce every gradient, wait, then
+        the streamed step with the gradients complete."""
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        produce(tt, passes)
+        producer.synchronize()
+        lst.lst_stream_step_devgrad(L.handle, ptrs, gptrs, buf0.data_ptr(), buf1.data_ptr(),
+                                    lst.adamw_hparams(step=tt, **hp_kw), None, 600_000)
+        torch.cuda.synchronize(device)
+        return time.perf_counter() - t0
+
+    prod_s = producer_alone(t, 1)
+    n_warm, t = warm_until_stable(lambda tt: overlapped(tt, 1), t)
+    e_steps = FRESH_GRAD_STEPS.get(args.workload, max(1, min(args.steps, args.e2e_steps)))
+    barrier(device)
+    times = []
+    for _ in range(e_steps):
+        times.append(overlapped(t, 1))
+        t += 1
+    t_dg = max_over_ranks(sum(times), device)
+    roof = max(prod_s, roof_link)
+    out = {"value": P_job * e_steps / t_dg, "unit": "params/s", "call": "lst_stream_step_devgrad_events",
+           "producer": "synth.device_fill_field, blocks n-1..0, one Backward-Done event per block",
+           "step_ms": 1e3 * t_dg / e_steps, "producer_alone_ms": 1e3 * prod_s, "link_roofline_ms": 1e3 * roof_link,
+           "roofline_ms": 1e3 * roof, "frac_of_roofline": roof / (t_dg / e_steps),
+           "h2d_bytes_per_step": dg_h2d, "d2h_bytes_per_step": d2h_b, "steps": e_steps, "warmup_steps": n_warm}
+    # the step with the gradients complete before the call (no producer in
+    # the timed region), for comparison
+    t0 = time.perf_counter()
+    lst.lst_stream_step_devgrad(L.handle, ptrs, gptrs, buf0.data_ptr(), buf1.data_ptr(),
+                                lst.adamw_hparams(step=t, **hp_kw), None, 600_000)
+    out["gradients_ready_step_ms"] = 1e3 * (time.perf_counter() - t0)
+    t += 1
+    # a producer as slow as a backward pass: calibrate its extra rounds
+    p_cal = 32
+    c_cal = producer_alone(t, p_cal, reps=1)
+    per_pass = max(1e-9, (c_cal - prod_s) / (p_cal - 1))
+    passes = int(max(1, min(20000, 1 + (0.8 * roof_link - prod_s) / per_pass)))
+    heavy_prod = producer_alone(t, passes, reps=1)
+    ov = overlapped(t, passes)
+    t += 1
+    se = serial(t, passes)
+    t += 1
+    stream_only = out["gradients_ready_step_ms"] / 1e3
+    out["heavy_producer"] = {"passes": passes, "producer_alone_ms": 1e3 * heavy_prod,
+                             "overlapped_step_ms": 1e3 * ov, "serial_ms": 1e3 * se,
+                             "max_ms": 1e3 * max(heavy_prod, roof_link),
+                             "sum_ms": 1e3 * (heavy_prod + stream_only),
+                             "frac_of_max": max(heavy_prod, roof_link) / ov}
+    del grads
+    out["next_t"] = t
+    return out
 
 
 def time_options_leg(args, L, dptrs, hp_kw, stream, device, world, t, flush, flush_rd, peak):

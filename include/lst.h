@@ -292,8 +292,8 @@ LST_API lst_status lst_adamw_step_ex_noalloc(const lst_layout* layout, void* con
    host_blocks: n_layers pointers to page-locked host memory (cudaHostAlloc,
    cudaHostRegister or lst_host_alloc), each 4096-byte aligned and at least
    the block's size. dev_buf0, dev_buf1: two device buffers, each 256-byte
-   aligned and at least max_block_bytes (lst_layout_info) long; block i is
-   staged in buffer i & 1, at the block's own offsets.
+   aligned and at least max_block_bytes (lst_layout_info) long; the k-th
+   block transferred is staged in buffer k & 1, at the block's own offsets.
    For each block, in sub-chunks of the layout's stream chunk size: the input
    prefix is copied host -> device on a copy stream, the update runs on a
    compute stream, and the output suffix is copied device -> host on a second
@@ -341,6 +341,30 @@ LST_API lst_status lst_stream_step_devgrad(const lst_layout* layout, void* const
                                            const void* const* dev_grads, void* dev_buf0, void* dev_buf1,
                                            const lst_adamw_hparams* hparams, const lst_step_options* opts,
                                            int64_t timeout_ms);
+
+/* The device-gradient streamed step overlapped with the backward pass that
+   produces the gradients ("MegaTrain" summary page, three-stream execution:
+   a Backward-Done event per layer releases that layer's gradient). Block i's
+   update waits, on the device, for grad_ready[i]: a cudaEvent_t that the
+   producer recorded on its own stream after writing dev_grads[i]. The state
+   of a block is copied in without waiting for it, so block i's state streams
+   in, is updated and streams out while gradients of later blocks in `order`
+   are still being produced; the host never waits for the producer.
+   grad_ready: host array of n_layers cudaEvent_t values (as void*); a NULL
+   entry means that block's gradient is already complete. Each event must
+   have been recorded before this call: the wait binds to its latest record
+   at the time of the call. The events are not modified.
+   order: host array holding a permutation of 0..n_layers-1, the order in
+   which blocks are transferred and updated (a backward pass completes its
+   layers last to first: order = n_layers-1, ..., 0), or NULL for index order.
+   Otherwise as lst_stream_step_devgrad; results are bit-identical to it.
+   Errors as lst_stream_step_devgrad, plus LST_ERR_INVALID_ARG when order is
+   not a permutation, and LST_ERR_CUDA when a wait on an event fails. */
+LST_API lst_status lst_stream_step_devgrad_events(const lst_layout* layout, void* const* host_blocks,
+                                                  const void* const* dev_grads, void* const* grad_ready,
+                                                  const int64_t* order, void* dev_buf0, void* dev_buf1,
+                                                  const lst_adamw_hparams* hparams, const lst_step_options* opts,
+                                                  int64_t timeout_ms);
 
 /* One AdamW step with the update kernel reading and writing the pinned host
    blocks in place over the host link (NVLink-C2C on Grace systems): no device

@@ -14,9 +14,13 @@
 // is moved in sub-chunks (the layout's stream chunk, default 16 Mi elements):
 // chunk c's update starts as soon as chunk c has arrived and its outbound copy
 // as soon as its update is done, so the pipeline fills and drains in one
-// sub-chunk rather than one whole block. Block i is staged in buffer i & 1 at
-// the block's own offsets; block i+2's inbound copies wait for the event that
-// block i's last outbound copy recorded. Events are re-recorded per chunk: a
+// sub-chunk rather than one whole block. The k-th block transferred is staged
+// in buffer k & 1 at the block's own offsets; the (k+2)-th block's inbound
+// copies wait for the event that the k-th block's last outbound copy recorded.
+// Blocks go in index order, or in a caller's order (a backward pass finishes
+// its layers last to first), and a block's update can wait for an event that
+// marks its gradient complete ("MegaTrain" page, three-stream execution: the
+// Backward-Done event). Events are re-recorded per chunk: a
 // stream wait binds to the most recent record enqueued before it, and all
 // enqueues come from this one host thread in order.
 #include <chrono>
@@ -250,7 +254,8 @@ using namespace lst;
 
 static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, void* dev_buf0, void* dev_buf1,
                               const lst_adamw_hparams* hp, const lst_step_options* opts,
-                              const void* const* dev_grads, int64_t timeout_ms) {
+                              const void* const* dev_grads, void* const* grad_ready, const int64_t* order,
+                              int64_t timeout_ms) {
   if (!Lc) return fail(LST_ERR_INVALID_ARG, "lst_stream_step: null layout");
   if (!hp) return fail(LST_ERR_INVALID_ARG, "lst_stream_step: null hparams");
   Scalars s;
@@ -280,6 +285,16 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
       return fail(LST_ERR_INVALID_ARG, "lst_stream_step: host block %lld is null", (long long)i);
     if (reinterpret_cast<uintptr_t>(host_blocks[i]) % 4096)
       return fail(LST_ERR_ALIGNMENT, "lst_stream_step: host block %lld not 4096-byte aligned", (long long)i);
+  }
+  if (order) {  // a permutation of the blocks
+    std::vector<char> seen((size_t)n, 0);
+    for (int64_t k = 0; k < n; ++k) {
+      const int64_t i = order[k];
+      if (i < 0 || i >= n || seen[(size_t)i])
+        return fail(LST_ERR_INVALID_ARG, "lst_stream_step: order is not a permutation of the %lld blocks (entry %lld)",
+                    (long long)n, (long long)k);
+      seen[(size_t)i] = 1;
+    }
   }
   if (dev_grads) {
     for (int64_t i = 0; i < n; ++i) {
@@ -344,25 +359,31 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
   bool used[2] = {false, false};
   const char* what = nullptr;
 
+  // Blocks in processing order; the k-th block that is transferred is staged
+  // in buffer k & 1.
+  auto block_at = [&](int64_t k) { return order ? order[k] : k; };
   int64_t first_active = -1, last_active = -1;
-  for (int64_t i = 0; i < n; ++i) {
+  for (int64_t k = 0; k < n; ++k) {
+    const int64_t i = block_at(k);
     if (skipped(i) || L->blocks[(size_t)i].padded == 0) continue;
     if (first_active < 0) first_active = i;
     last_active = i;
   }
-  for (int64_t i = 0; i < n && !what; ++i) {
+  int64_t staged = 0;
+  for (int64_t k = 0; k < n && !what; ++k) {
+    const int64_t i = block_at(k);
     const Block& b = L->blocks[(size_t)i];
     if (skipped(i)) continue;  // a locked block: no transfer, no update
     if (b.padded == 0) {
       if (want_sq) {  // an empty block's sum of squares is 0
-        LaunchOp l{L->fmt, block_run(*L, b, bufs[(int)(i & 1)], 0, 0), &s, E->compute, true, {}, opts->workspace,
+        LaunchOp l{L->fmt, block_run(*L, b, bufs[0], 0, 0), &s, E->compute, true, {}, opts->workspace,
                    opts->grad_sq};
         l.run_ex = RunEx{l.run, bc1[(size_t)i], bc2[(size_t)i], (int32_t)i, 0};
         if ((err = enq(do_launch, &l)) != cudaSuccess) { what = "launch update"; break; }
       }
       continue;
     }
-    const int bi = (int)(i & 1);
+    const int bi = (int)(staged++ & 1);
     char* buf = bufs[bi];
     char* host = static_cast<char*>(host_blocks[i]);
     // the SMs reach the host block through its device mapping
@@ -375,6 +396,10 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
       if ((err = enq(do_wait, &w)) != cudaSuccess) { what = "wait buffer-free"; break; }
     }
     used[bi] = true;
+    if (grad_ready && grad_ready[i]) {  // Backward-Done: the block's gradient is complete
+      RecordOp w{static_cast<cudaEvent_t>(grad_ready[i]), E->compute};
+      if ((err = enq(do_wait, &w)) != cudaSuccess) { what = "wait gradient-ready"; break; }
+    }
     const int64_t C = (L->stream_chunk > 0 && L->stream_chunk < b.padded) ? L->stream_chunk : b.padded;
     const bool whole = (C == b.padded);
     const std::vector<int64_t> cuts = chunk_cuts(b.padded, C, i == first_active, i == last_active);
@@ -472,14 +497,14 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
 extern "C" lst_status lst_stream_step(const lst_layout* L, void* const* host_blocks, void* dev_buf0, void* dev_buf1,
                                       const lst_adamw_hparams* hp, int64_t timeout_ms) {
   clear_error();
-  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, nullptr, nullptr, timeout_ms);
+  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, nullptr, nullptr, nullptr, nullptr, timeout_ms);
 }
 
 extern "C" lst_status lst_stream_step_ex(const lst_layout* L, void* const* host_blocks, void* dev_buf0,
                                          void* dev_buf1, const lst_adamw_hparams* hp, const lst_step_options* opts,
                                          int64_t timeout_ms) {
   clear_error();
-  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, opts, nullptr, timeout_ms);
+  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, opts, nullptr, nullptr, nullptr, timeout_ms);
 }
 
 extern "C" lst_status lst_stream_step_devgrad(const lst_layout* L, void* const* host_blocks,
@@ -489,5 +514,16 @@ extern "C" lst_status lst_stream_step_devgrad(const lst_layout* L, void* const* 
   clear_error();
   if (L && !L->blocks.empty() && !dev_grads)
     return fail(LST_ERR_INVALID_ARG, "lst_stream_step_devgrad: dev_grads is null");
-  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, opts, dev_grads, timeout_ms);
+  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, opts, dev_grads, nullptr, nullptr, timeout_ms);
+}
+
+extern "C" lst_status lst_stream_step_devgrad_events(const lst_layout* L, void* const* host_blocks,
+                                                     const void* const* dev_grads, void* const* grad_ready,
+                                                     const int64_t* order, void* dev_buf0, void* dev_buf1,
+                                                     const lst_adamw_hparams* hp, const lst_step_options* opts,
+                                                     int64_t timeout_ms) {
+  clear_error();
+  if (L && !L->blocks.empty() && !dev_grads)
+    return fail(LST_ERR_INVALID_ARG, "lst_stream_step_devgrad_events: dev_grads is null");
+  return stream_impl(L, host_blocks, dev_buf0, dev_buf1, hp, opts, dev_grads, grad_ready, order, timeout_ms);
 }

@@ -111,6 +111,8 @@ def lib() -> ctypes.CDLL:
             "lst_workspace_bytes": ([], i64),
             "lst_stream_step_devgrad": ([vp, P(vp), P(vp), vp, vp, P(lst_adamw_hparams), P(lst_step_options), i64],
                                         ctypes.c_int),
+            "lst_stream_step_devgrad_events": ([vp, P(vp), P(vp), P(vp), vp, vp, vp, P(lst_adamw_hparams),
+                                                P(lst_step_options), i64], ctypes.c_int),
             "lst_adamw_step_ex_noalloc": ([vp, P(vp), P(lst_adamw_hparams), vp, vp, vp, vp], ctypes.c_int),
             "lst_host_alloc": ([i64, P(vp)], ctypes.c_int),
             "lst_host_free": ([vp], ctypes.c_int),
@@ -266,6 +268,19 @@ def lst_stream_step_devgrad(handle: int, host_blocks: Sequence[int], dev_grads: 
     _check(lib().lst_stream_step_devgrad(handle, _ptr_array(host_blocks), _ptr_array(dev_grads), dev_buf0, dev_buf1,
                                          ctypes.byref(hparams), ctypes.byref(opts) if opts is not None else None,
                                          timeout_ms))
+
+
+def lst_stream_step_devgrad_events(handle: int, host_blocks: Sequence[int], dev_grads: Sequence[int],
+                                   grad_ready: Sequence[int], order, dev_buf0: int, dev_buf1: int,
+                                   hparams: lst_adamw_hparams, opts=None, timeout_ms: int = 0) -> None:
+    """grad_ready: cudaEvent_t values as ints (0 for a gradient already
+    complete), e.g. torch.cuda.Event.cuda_event; order: block indices or None."""
+    ords = (ctypes.c_int64 * max(1, len(order)))(*[int(x) for x in order]) if order is not None else None
+    _check(lib().lst_stream_step_devgrad_events(handle, _ptr_array(host_blocks), _ptr_array(dev_grads),
+                                                _ptr_array(grad_ready),
+                                                ctypes.cast(ords, ctypes.c_void_p) if ords is not None else None,
+                                                dev_buf0, dev_buf1, ctypes.byref(hparams),
+                                                ctypes.byref(opts) if opts is not None else None, timeout_ms))
 
 
 def lst_store_create(layout: int, directory: str, host_blocks=None, step: int = 0) -> int:

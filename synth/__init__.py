@@ -24,7 +24,9 @@ from . import shapes  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libsynth.so")
+_DEV_LIB_PATH = os.path.join(_HERE, "libsynth_dev.so")
 _lib = None
+_dev_lib = None
 
 # Field codes used in stream ids.
 FIELD_W, FIELD_G, FIELD_M, FIELD_V, FIELD_MASTER = 1, 2, 3, 4, 5
@@ -56,6 +58,23 @@ def lib():
         L.synth_gather.restype = ci
         _lib = L
     return _lib
+
+
+def dev_lib():
+    """The generator on the GPU (gen_dev.cu): a gradient producer that stands
+    in for a backward pass. Raises if it has not been built."""
+    global _dev_lib
+    if _dev_lib is None:
+        if not os.path.exists(_DEV_LIB_PATH):
+            raise RuntimeError(f"{_DEV_LIB_PATH} is missing: run synth.build.build()")
+        L = ctypes.CDLL(_DEV_LIB_PATH)
+        u64, i64, f32, vp, ci = ctypes.c_uint64, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
+        L.synth_dev_fill.argtypes = [ci, u64, u64, u64, i64, f32, vp, ci, vp]
+        L.synth_dev_fill.restype = ci
+        L.synth_dev_zero.argtypes = [vp, i64, vp]
+        L.synth_dev_zero.restype = ci
+        _dev_lib = L
+    return _dev_lib
 
 
 def scale_for(sigma: float) -> np.float32:
@@ -189,3 +208,31 @@ def gather_block(field: str, fmt: str, spans: Sequence[Tuple[str, int, int]], la
         s = g_seed if (field == "G" and g_seed is not None) else seed
         out[sel] = gather(_kind(dist, dtype), s, stream_id(FIELD_CODES[field], layer), idx[sel], sigma)
     return out
+
+
+def device_fill_field(dev_ptr: int, field: str, fmt: str, spans: Sequence[Tuple[str, int, int]], padded: int,
+                      layer: int, workload: str, t: int, seed: int = DEFAULT_SEED, stream: int = 0,
+                      passes: int = 1) -> None:
+    """The GPU twin of fill_field: one field of a block written into device
+    memory at dev_ptr (padded elements; padding and zero-valued tensors set to
+    zero), enqueued on the CUDA stream `stream` (a cudaStream_t as an int).
+    passes > 1 adds hash rounds per element that stand in for the compute of
+    a backward pass; the values do not depend on it."""
+    dtype = dict(FORMAT_FIELDS[fmt])[field]
+    esz = 2 if dtype == "bf16" else 4
+    L = dev_lib()
+    rc = L.synth_dev_zero(dev_ptr, padded * esz, stream or None)
+    if rc != 0:
+        raise RuntimeError(f"synth_dev_zero failed ({rc})")
+    if fmt == "L16M" and field == "W":
+        return
+    for (name, off, n) in spans:
+        if n == 0:
+            continue
+        dist, sigma = field_dist(workload, field, name, t)
+        if dist == "zero":
+            continue
+        rc = L.synth_dev_fill(_kind(dist, dtype), seed & (2 ** 64 - 1), stream_id(FIELD_CODES[field], layer), off,
+                              n, float(scale_for(sigma)), dev_ptr + off * esz, int(passes), stream or None)
+        if rc != 0:
+            raise RuntimeError(f"synth_dev_fill failed ({rc})")

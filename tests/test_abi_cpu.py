@@ -191,6 +191,31 @@ def test_step_options_validation_before_any_cuda_call(L):
         L.lst_layout_destroy(h)
 
 
+def test_gradient_event_step_validation_before_any_cuda_call(L):
+    """lst_stream_step_devgrad_events refuses an order that is not a
+    permutation of the blocks, and missing gradients, before any CUDA call
+    (the pointers below are never dereferenced)."""
+    h = L.lst_layout_create([(8,), (8,), (8,)], [0, 1, 2], "L12")
+    try:
+        hosts, grads, evs = [4096, 8192, 12288], [256, 512, 768], [0, 0, 0]
+        for order in ([0, 0, 1], [0, 1, 3], [2, 1, -1]):
+            with pytest.raises(L.LstError) as e:
+                L.lst_stream_step_devgrad_events(h, hosts, grads, evs, order, 4096, 8192, L.adamw_hparams())
+            assert e.value.status == L.LST_ERR_INVALID_ARG and "permutation" in str(e.value)
+        with pytest.raises(L.LstError) as e:  # a gradient pointer missing
+            L.lst_stream_step_devgrad_events(h, hosts, [256, 0, 768], evs, [2, 1, 0], 4096, 8192,
+                                             L.adamw_hparams())
+        assert e.value.status == L.LST_ERR_INVALID_ARG
+        with pytest.raises(L.LstError) as e:  # a misaligned gradient
+            L.lst_stream_step_devgrad_events(h, hosts, [256, 520, 768], evs, None, 4096, 8192, L.adamw_hparams())
+        assert e.value.status == L.LST_ERR_ALIGNMENT
+        r = L.lib().lst_stream_step_devgrad_events(h, L._ptr_array(hosts), None, L._ptr_array(evs), None,
+                                                   4096, 8192, ctypes.byref(L.adamw_hparams()), None, 0)
+        assert r == L.LST_ERR_INVALID_ARG  # no gradients at all
+    finally:
+        L.lst_layout_destroy(h)
+
+
 def test_bench_runs_the_oracle_only_in_its_baseline_and_reference_legs():
     """bench.py imports the oracle only inside the CPU-baseline helpers and the
     reference arm, and calls those helpers only from the baseline leg (rank 0,
