@@ -612,26 +612,28 @@ def block_h2d_rates(torch, arrs, dev):
     return out
 
 
-def heal_pinned_state(torch, L, ptrs, arrs, dev, tries: int = 3, max_extra_bytes: int = 40 << 30):
+def heal_pinned_state(torch, L, ptrs, arrs, dev, tries: int = 3, max_extra_bytes: int = 40 << 30,
+                      frac: float = 0.85, rates=None):
     """Health check of the pinned state blocks. On the GB300 hosts here, some
-    pinned allocations are read by the copy engines at a few GB/s instead of
-    the link rate, for their whole lifetime (more of them after other
-    processes have pinned and freed a lot of memory). A block whose
-    host-to-device rate is under half the best block's is copied into a fresh
-    allocation, up to `tries` times; replaced allocations stay pinned until
-    the caller frees them (returned), so the allocator does not hand the same
-    pages straight back. Returns (slow blocks before, blocks replaced,
+    pinned allocations are read by the copy engines at a fraction of the link
+    rate (a few GB/s to about half), for their whole lifetime (more of them
+    after other processes have pinned and freed a lot of memory), and the
+    slowest block sets the pace of a streamed step. A block whose
+    host-to-device rate is under `frac` of the best block's is copied into a
+    fresh allocation, up to `tries` times; replaced allocations stay pinned
+    until the caller frees them (returned), so the allocator does not hand the
+    same pages straight back. Returns (slow blocks before, blocks replaced,
     allocations to free)."""
     import ctypes
     import numpy as np
     from optimizer_update_gb300 import lst
-    rates = block_h2d_rates(torch, arrs, dev)
+    rates = rates if rates is not None else block_h2d_rates(torch, arrs, dev)
     ref = max(rates)
-    slow_before = sum(1 for r in rates if r < 0.5 * ref)
+    slow_before = sum(1 for r in rates if r < frac * ref)
     retired, healed, extra = [], 0, 0
     for i, r in enumerate(rates):
         k = 0
-        while r < 0.5 * ref and k < tries:
+        while r < frac * ref and k < tries:
             n = arrs[i].size
             if extra + n > max_extra_bytes:
                 break
@@ -914,7 +916,7 @@ def run_ours(args):
                        "note": "first three calls on the pinned blocks as allocated (lst_host_alloc), "
                                "before slow allocations are replaced",
                        "block_h2d_gbs_min": min(rates_before),
-                       "slow_blocks": sum(1 for r in rates_before if r < 0.5 * max(rates_before))}
+                       "slow_blocks": sum(1 for r in rates_before if r < 0.85 * max(rates_before))}
     slow_before_heal, healed, retired = heal_pinned_state(torch, L, ptrs, arrs, buf0)
     a0, a1 = probe_pair()
     link = link_bandwidth(torch, [a0, a1], buf0, buf1, nb)
@@ -934,8 +936,13 @@ def run_ours(args):
     else:
         t_first = t
     # every block's own host-to-device rate, right before the timed steps
-    # (a slow pinned allocation holds up the pipeline)
+    # (a slow pinned allocation holds up the pipeline): a block that has
+    # become slow since the health check is replaced as well
     block_rates = block_h2d_rates(torch, arrs, buf0)
+    slow_late, healed_late, retired_late = heal_pinned_state(torch, L, ptrs, arrs, buf0, rates=block_rates)
+    retired += retired_late
+    if healed_late:
+        block_rates = block_h2d_rates(torch, arrs, buf0)
     step_times = []
     for k in range(n_stream):
         tt = t_first + k
@@ -966,8 +973,9 @@ def run_ours(args):
                        chunk_elems=chunk, warmup_steps=stream_warm,
                        host_huge_page_bytes=huge_bytes, host_state_bytes=state_bytes,
                        block_h2d_gbs_min=min(block_rates), block_h2d_gbs_median=statistics.median(block_rates),
-                       slow_blocks=sum(1 for r in block_rates if r < 0.5 * link["h2d_gbs"]),
+                       slow_blocks=sum(1 for r in block_rates if r < 0.85 * max(block_rates)),
                        slow_blocks_before_heal=slow_before_heal, healed_blocks=healed,
+                       slow_blocks_before_timed_steps=slow_late, healed_before_timed_steps=healed_late,
                        link_before_heal={k: link_before[k] for k in ("h2d_gbs", "d2h_gbs", "h2d_concurrent_gbs",
                                                                      "d2h_concurrent_gbs")})
 

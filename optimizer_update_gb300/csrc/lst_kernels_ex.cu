@@ -17,10 +17,11 @@ namespace lst {
 // GSQ=true also return sum(g^2) over every run as a by-product of the same
 // pass: per task each lane adds its 8 squares in fp32 (exact products for bf16
 // g) and accumulates tasks in an fp32 pair with exact error recovery (below);
-// a warp reduces its lanes in fp64 in a fixed shuffle order, a CTA adds its
-// warps' sums per run in warp order and writes one partial per run to the
-// workspace, and a second small launch adds each run's partials in a fixed
-// order. The result is deterministic for a given grid.
+// a warp reduces its lanes' pairs in a fixed shuffle order, a CTA adds its
+// warps' pairs per run in warp order and writes one partial pair per run to
+// the workspace, and a second small launch adds each run's partials in a fixed
+// order and forms the fp64 result. The result is deterministic for a given
+// grid.
 // Large launches walk run by run with the main kernel's prefetch schedule;
 // small ones (many short runs, e.g. LoRA adapters) walk their global tasks
 // across runs with a cursor, as the main small-launch kernel.
@@ -87,12 +88,34 @@ __device__ __forceinline__ double sum_pair_value(const SumPair& p) {
   return isfinite(p.hi) ? (double)p.hi + (double)p.lo : (double)p.hi;
 }
 
-// Sum over the warp's lanes in a fixed butterfly order (every lane gets it).
-__device__ __forceinline__ double warp_sum_f64(double x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
+// The sum of two pairs as a pair: the high parts are added with their exact
+// rounding error (TwoSum), the low parts and that error in fp32, and the
+// result renormalised (the larger part first). About 2^-44 relative error for
+// nonnegative terms, fp32 operations only: this GPU's fp64 rate is a small
+// fraction of its fp32 rate, and a warp-wide fp64 reduction per run and warp
+// cost several microseconds of a 27 us small launch. Commutative bit for bit
+// (TwoSum's error term does not depend on the operand order), so a butterfly
+// leaves the same value in every lane. An infinite or NaN sum is kept as is.
+__device__ __forceinline__ SumPair pair_add(const SumPair& a, const SumPair& b) {
+  const float s = __fadd_rn(a.hi, b.hi);
+  if (!isfinite(s)) return SumPair{s, 0.0f};
+  const float bb = __fsub_rn(s, a.hi);
+  const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
+  const float t = __fadd_rn(__fadd_rn(a.lo, b.lo), e);
+  const float hi = __fadd_rn(s, t);
+  return SumPair{hi, __fsub_rn(t, __fsub_rn(hi, s))};
 }
+
+// Sum of the warp's lanes' pairs in a fixed butterfly order (every lane gets it).
+__device__ __forceinline__ SumPair warp_sum_pair(SumPair p) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const SumPair q{__shfl_xor_sync(0xffffffffu, p.hi, o), __shfl_xor_sync(0xffffffffu, p.lo, o)};
+    p = pair_add(p, q);
+  }
+  return p;
+}
+
 
 // Programmatic dependent launch (PTX griddepcontrol): the update grid's CTAs
 // signal once their partial sums are written, so the reduce grid that follows
@@ -110,10 +133,14 @@ __device__ __forceinline__ void wait_for_prerequisite_grid() {
 }
 
 // Second launch of a step with sums: one CTA per run adds that run's partials
-// (one per CTA of the update launch; thread k takes partials k, k + 256, ...
-// in that order) and its threads' sums in a fixed order. A separate launch
-// needs no ticket counter, fence or workspace initialisation, and reads every
-// partial in one or a few rounds.
+// (one pair per CTA of the update launch; thread k takes partials k, k + 256,
+// ... in that order) and its threads' sums in a fixed order, as fp32 pairs:
+// only the final value is formed in fp64 (fp64 operations are slow on this
+// GPU, and this launch's dependent chain of them made it several microseconds
+// long). A separate launch needs no ticket counter, fence or workspace
+// initialisation. (Tickets taken by the update CTAs, with the last CTA adding
+// a run's partials, were measured slower: each CTA's fence waits for its own
+// streaming stores.)
 struct GradSqTable {
   int32_t n;                  // runs of the update launch
   int32_t partials_per_run;   // CTAs of the update launch
@@ -122,29 +149,27 @@ struct GradSqTable {
 };
 
 __global__ void __launch_bounds__(kThreads) lst_grad_sq_reduce_kernel(const __grid_constant__ GradSqTable t,
-                                                                     const double* partials, double* grad_sq) {
-  __shared__ double warp_total[kThreads / 32];
+                                                                     const SumPair* partials, double* grad_sq) {
+  __shared__ SumPair warp_total[kThreads / 32];
   wait_for_prerequisite_grid();
   const int r = blockIdx.x;
   const int out = t.out_index[r];
   if (out < 0) return;  // the whole CTA
-  const double* p = partials + (size_t)r * t.partials_per_run;
-  double a[4] = {0.0, 0.0, 0.0, 0.0};
-  for (int c0 = 0; c0 < t.partials_per_run; c0 += 4 * kThreads) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int c = c0 + threadIdx.x + k * kThreads;
-      if (c < t.partials_per_run) a[k] += __ldcg(p + c);  // from L2: written by the other grid
-    }
+  const float2* p = reinterpret_cast<const float2*>(partials) + (size_t)r * t.partials_per_run;
+  SumPair a{0.0f, 0.0f};
+  for (int c = threadIdx.x; c < t.partials_per_run; c += kThreads) {
+    const float2 x = __ldcg(p + c);  // from L2: written by the other grid
+    a = pair_add(a, SumPair{x.x, x.y});
   }
-  const double x = warp_sum_f64((a[0] + a[1]) + (a[2] + a[3]));
-  if ((threadIdx.x & 31) == 0) warp_total[threadIdx.x >> 5] = x;
+  const SumPair w = warp_sum_pair(a);
+  if ((threadIdx.x & 31) == 0) warp_total[threadIdx.x >> 5] = w;
   __syncthreads();
   if (threadIdx.x == 0) {
-    double sum = 0.0;
+    SumPair sum = warp_total[0];
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) sum += warp_total[w];
-    grad_sq[out] = t.accumulate[r] ? grad_sq[out] + sum : sum;
+    for (int k = 1; k < kThreads / 32; ++k) sum = pair_add(sum, warp_total[k]);
+    const double v = sum_pair_value(sum);
+    grad_sq[out] = t.accumulate[r] ? grad_sq[out] + v : v;
   }
 }
 
@@ -158,8 +183,8 @@ __global__ void __launch_bounds__(kThreads) lst_grad_sq_reduce_kernel(const __gr
 // CTA per SM let the compiler take 112 and measured 0.922).
 template <int FMT, bool GSQ>
 __global__ void __launch_bounds__(kThreads, (FMT == F_L12 ? 3 : 0))
-    lst_update_ex_kernel(const __grid_constant__ RunTableEx tab, const Scalars s0, double* partials) {
-  __shared__ double warp_sum[kThreads / 32];
+    lst_update_ex_kernel(const __grid_constant__ RunTableEx tab, const Scalars s0, SumPair* partials) {
+  __shared__ SumPair warp_sum[kThreads / 32];
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   const long long n_warps = (long long)gridDim.x * (kThreads / 32);
@@ -196,13 +221,13 @@ __global__ void __launch_bounds__(kThreads, (FMT == F_L12 ? 3 : 0))
       }
     }
     if (GSQ) {
-      const double lane_sum = warp_sum_f64(sum_pair_value(acc));
-      if (lane == 0) warp_sum[wid] = lane_sum;
+      const SumPair ws = warp_sum_pair(acc);
+      if (lane == 0) warp_sum[wid] = ws;
       __syncthreads();
       if (threadIdx.x == 0) {
-        double c = 0.0;
+        SumPair c = warp_sum[0];
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) c += warp_sum[w];
+        for (int w = 1; w < kThreads / 32; ++w) c = pair_add(c, warp_sum[w]);
         partials[(size_t)r * gridDim.x + blockIdx.x] = c;
       }
       __syncthreads();
@@ -220,13 +245,14 @@ __global__ void __launch_bounds__(kThreads, (FMT == F_L12 ? 3 : 0))
 // warp order.
 template <int FMT, bool GSQ>
 __global__ void __launch_bounds__(kThreads, 4)
-    lst_update_ex_small_kernel(const __grid_constant__ RunTableEx tab, const Scalars s0, double* partials,
+    lst_update_ex_small_kernel(const __grid_constant__ RunTableEx tab, const Scalars s0, SumPair* partials,
                                const long long total_tasks) {
-  __shared__ double run_sum[GSQ ? kThreads / 32 : 1][GSQ ? kMaxRunsPerLaunch : 1];
+  __shared__ SumPair run_sum[GSQ ? kThreads / 32 : 1][GSQ ? kMaxRunsPerLaunch : 1];
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   if (GSQ) {
-    for (int i = threadIdx.x; i < (kThreads / 32) * kMaxRunsPerLaunch; i += kThreads) (&run_sum[0][0])[i] = 0.0;
+    for (int i = threadIdx.x; i < (kThreads / 32) * kMaxRunsPerLaunch; i += kThreads)
+      (&run_sum[0][0])[i] = SumPair{0.0f, 0.0f};
     __syncthreads();
   }
   const long long n_warps = (long long)gridDim.x * (kThreads / 32);
@@ -238,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 4)
   for (; g < total_tasks; g += n_warps) {
     if (g >= end) {  // warp-uniform: g is the same in every lane
       if (GSQ && r >= 0) {
-        const double warp_total = warp_sum_f64(sum_pair_value(acc));
+        const SumPair warp_total = warp_sum_pair(acc);
         if (lane == 0) run_sum[wid][r] = warp_total;
         acc = SumPair{0.0f, 0.0f};
       }
@@ -261,14 +287,14 @@ __global__ void __launch_bounds__(kThreads, 4)
   }
   if (GSQ) {
     if (r >= 0) {
-      const double warp_total = warp_sum_f64(sum_pair_value(acc));
+      const SumPair warp_total = warp_sum_pair(acc);
       if (lane == 0) run_sum[wid][r] = warp_total;
     }
     __syncthreads();
     for (int q = threadIdx.x; q < tab.n; q += kThreads) {
-      double c = 0.0;
+      SumPair c = run_sum[0][q];
 #pragma unroll
-      for (int w = 0; w < kThreads / 32; ++w) c += run_sum[w][q];
+      for (int w = 1; w < kThreads / 32; ++w) c = pair_add(c, run_sum[w][q]);
       partials[(size_t)q * gridDim.x + blockIdx.x] = c;
     }
     allow_dependent_launch();
@@ -288,8 +314,8 @@ static std::mutex g_dev_ex_mu;
 // the main path: about twice the L2).
 constexpr long long kSmallLaunchBytesEx = 256ll << 20;
 
-typedef void (*KernelExFn)(const RunTableEx, const Scalars, double*);
-typedef void (*KernelExSmallFn)(const RunTableEx, const Scalars, double*, const long long);
+typedef void (*KernelExFn)(const RunTableEx, const Scalars, SumPair*);
+typedef void (*KernelExSmallFn)(const RunTableEx, const Scalars, SumPair*, const long long);
 
 static KernelExFn kernel_ex_for(lst_format fmt, bool gsq) {
   switch (fmt) {
@@ -336,7 +362,7 @@ cudaError_t launch_update_ex(lst_format fmt, const RunEx* runs, int n_runs, cons
                              double* grad_sq, cudaStream_t stream) {
   const bool gsq = grad_sq != nullptr;
   const FormatInfo& fi = format_info(fmt);
-  double* partials = gsq ? reinterpret_cast<double*>(static_cast<char*>(workspace) + kWorkspaceHeader) : nullptr;
+  SumPair* partials = gsq ? reinterpret_cast<SumPair*>(static_cast<char*>(workspace) + kWorkspaceHeader) : nullptr;
   int i = 0;
   while (i < n_runs) {
     RunTableEx tab;
@@ -399,7 +425,7 @@ cudaError_t launch_update_ex(lst_format fmt, const RunEx* runs, int n_runs, cons
       attr[0].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      err = cudaLaunchKernelEx(&cfg, lst_grad_sq_reduce_kernel, t, static_cast<const double*>(partials), grad_sq);
+      err = cudaLaunchKernelEx(&cfg, lst_grad_sq_reduce_kernel, t, static_cast<const SumPair*>(partials), grad_sq);
       if (err != cudaSuccess) return err;
     }
   }
