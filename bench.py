@@ -593,47 +593,60 @@ def layout_config(L, workload, world, max_blocks=0, shard=False, params_job=None
                       max_blocks, shard, params_job)
 
 
-def block_h2d_rates(torch, arrs, dev):
-    """Host-to-device rate of each pinned block, one whole-block copy each
-    (GB/s, CUDA events on one stream): on a host where some pinned
-    allocations are slow, this names them."""
+def block_link_rates(torch, arrs, dev):
+    """Host-to-device and device-to-host rate of each pinned block, one
+    whole-block copy each way (GB/s, CUDA events on one stream; the copy back
+    writes the bytes the first copy just read): on a host where some pinned
+    allocations are slow, in either direction, this names them. Returns
+    (h2d rates, d2h rates)."""
     s = torch.cuda.Stream()
-    out = []
+    h2d, d2h = [], []
     for a in arrs:
         n = a.size
         h = torch.from_numpy(a)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         with torch.cuda.stream(s):
-            e0.record(s)
+            e[0].record(s)
             dev[:n].copy_(h, non_blocking=True)
-            e1.record(s)
-        e1.synchronize()
-        out.append(n / (e0.elapsed_time(e1) / 1e3) / 1e9)
-    return out
+            e[1].record(s)
+            h.copy_(dev[:n], non_blocking=True)
+            e[2].record(s)
+        e[2].synchronize()
+        h2d.append(n / (e[0].elapsed_time(e[1]) / 1e3) / 1e9)
+        d2h.append(n / (e[1].elapsed_time(e[2]) / 1e3) / 1e9)
+    return h2d, d2h
+
+
+def slow_block_flags(rates, frac: float = 0.85):
+    """Per block: is either direction under `frac` of the best block's rate?"""
+    h2d, d2h = rates
+    return [r < frac * max(h2d) or q < frac * max(d2h) for r, q in zip(h2d, d2h)]
 
 
 def heal_pinned_state(torch, L, ptrs, arrs, dev, tries: int = 3, max_extra_bytes: int = 40 << 30,
                       frac: float = 0.85, rates=None):
     """Health check of the pinned state blocks. On the GB300 hosts here, some
-    pinned allocations are read by the copy engines at a fraction of the link
+    pinned allocations are moved by the copy engines at a fraction of the link
     rate (a few GB/s to about half), for their whole lifetime (more of them
     after other processes have pinned and freed a lot of memory), and the
     slowest block sets the pace of a streamed step. A block whose
-    host-to-device rate is under `frac` of the best block's is copied into a
-    fresh allocation, up to `tries` times; replaced allocations stay pinned
-    until the caller frees them (returned), so the allocator does not hand the
-    same pages straight back. Returns (slow blocks before, blocks replaced,
-    allocations to free)."""
+    host-to-device or device-to-host rate is under `frac` of the best block's
+    in that direction is copied into a fresh allocation, up to `tries` times;
+    replaced allocations stay pinned until the caller frees them (returned),
+    so the allocator does not hand the same pages straight back. Returns (slow
+    blocks before, blocks replaced, allocations to free)."""
     import ctypes
     import numpy as np
     from optimizer_update_gb300 import lst
-    rates = rates if rates is not None else block_h2d_rates(torch, arrs, dev)
-    ref = max(rates)
-    slow_before = sum(1 for r in rates if r < frac * ref)
+    rates = rates if rates is not None else block_link_rates(torch, arrs, dev)
+    best_h2d, best_d2h = max(rates[0]), max(rates[1])
+    slow = slow_block_flags(rates, frac)
+    slow_before = sum(slow)
     retired, healed, extra = [], 0, 0
-    for i, r in enumerate(rates):
+    for i in range(len(arrs)):
         k = 0
-        while r < frac * ref and k < tries:
+        bad = slow[i]
+        while bad and k < tries:
             n = arrs[i].size
             if extra + n > max_extra_bytes:
                 break
@@ -643,7 +656,8 @@ def heal_pinned_state(torch, L, ptrs, arrs, dev, tries: int = 3, max_extra_bytes
             retired.append(ptrs[i])
             ptrs[i], arrs[i] = p, a
             extra += n
-            r = block_h2d_rates(torch, [a], dev)[0]
+            h, d = block_link_rates(torch, [a], dev)
+            bad = h[0] < frac * best_h2d or d[0] < frac * best_d2h
             k += 1
         if k:
             healed += 1
@@ -907,7 +921,7 @@ def run_ours(args):
         stream_call(t)
         t += 1
         pre.append(time.perf_counter() - t0w)
-    rates_before = block_h2d_rates(torch, arrs, buf0)
+    rates_before = block_link_rates(torch, arrs, buf0)
     roof_before = max(h2d_b / (link_before["h2d_concurrent_gbs"] * 1e9),
                       d2h_b / (link_before["d2h_concurrent_gbs"] * 1e9))
     e2e_before_heal = {"value": P_job / statistics.median(pre), "unit": "params/s", "call": "lst_stream_step",
@@ -915,8 +929,8 @@ def run_ours(args):
                        "frac_of_link_roofline": roof_before / statistics.median(pre),
                        "note": "first three calls on the pinned blocks as allocated (lst_host_alloc), "
                                "before slow allocations are replaced",
-                       "block_h2d_gbs_min": min(rates_before),
-                       "slow_blocks": sum(1 for r in rates_before if r < 0.85 * max(rates_before))}
+                       "block_h2d_gbs_min": min(rates_before[0]), "block_d2h_gbs_min": min(rates_before[1]),
+                       "slow_blocks": sum(slow_block_flags(rates_before))}
     slow_before_heal, healed, retired = heal_pinned_state(torch, L, ptrs, arrs, buf0)
     a0, a1 = probe_pair()
     link = link_bandwidth(torch, [a0, a1], buf0, buf1, nb)
@@ -935,14 +949,14 @@ def run_ours(args):
         t_first = 1
     else:
         t_first = t
-    # every block's own host-to-device rate, right before the timed steps
-    # (a slow pinned allocation holds up the pipeline): a block that has
-    # become slow since the health check is replaced as well
-    block_rates = block_h2d_rates(torch, arrs, buf0)
+    # every block's own rates both ways, right before the timed steps (a
+    # slow pinned allocation holds up the pipeline): a block that has become
+    # slow since the health check is replaced as well
+    block_rates = block_link_rates(torch, arrs, buf0)
     slow_late, healed_late, retired_late = heal_pinned_state(torch, L, ptrs, arrs, buf0, rates=block_rates)
     retired += retired_late
     if healed_late:
-        block_rates = block_h2d_rates(torch, arrs, buf0)
+        block_rates = block_link_rates(torch, arrs, buf0)
     step_times = []
     for k in range(n_stream):
         tt = t_first + k
@@ -972,8 +986,9 @@ def run_ours(args):
                        roofline_ms=1e3 * roof_t, frac_of_link_roofline=roof_t / (t_e2e / n_stream),
                        chunk_elems=chunk, warmup_steps=stream_warm,
                        host_huge_page_bytes=huge_bytes, host_state_bytes=state_bytes,
-                       block_h2d_gbs_min=min(block_rates), block_h2d_gbs_median=statistics.median(block_rates),
-                       slow_blocks=sum(1 for r in block_rates if r < 0.85 * max(block_rates)),
+                       block_h2d_gbs_min=min(block_rates[0]), block_h2d_gbs_median=statistics.median(block_rates[0]),
+                       block_d2h_gbs_min=min(block_rates[1]), block_d2h_gbs_median=statistics.median(block_rates[1]),
+                       slow_blocks=sum(slow_block_flags(block_rates)),
                        slow_blocks_before_heal=slow_before_heal, healed_blocks=healed,
                        slow_blocks_before_timed_steps=slow_late, healed_before_timed_steps=healed_late,
                        link_before_heal={k: link_before[k] for k in ("h2d_gbs", "d2h_gbs", "h2d_concurrent_gbs",

@@ -232,8 +232,8 @@ typedef struct lst_step_options {
 } lst_step_options;
 
 /* Bytes of device workspace the sum-of-squares reduction needs (a constant:
-   one fp64 partial per CTA, up to 1024 CTAs, and per block of one launch, up
-   to 128 blocks, after a reserved 256-byte header). */
+   one 8-byte partial sum per CTA, up to 1024 CTAs, and per block of one
+   launch, up to 128 blocks, after a reserved 256-byte header). */
 LST_API int64_t lst_workspace_bytes(void);
 
 /* lst_adamw_step with per-block options (opts may be NULL). Results of a

@@ -132,7 +132,7 @@ inline int launch_waves(lst_format fmt, long long bytes) {
 }
 
 // Workspace of the sum-of-squares reduction: a reserved 256-byte header, then
-// one fp64 partial per (run, CTA) of a launch.
+// one partial sum (a pair of fp32 values, 8 bytes) per (run, CTA) of a launch.
 constexpr int kMaxGridEx = 1024;
 constexpr int64_t kWorkspaceHeader = 256;
 constexpr int64_t kWorkspaceBytes = kWorkspaceHeader + int64_t(8) * kMaxGridEx * kMaxRunsPerLaunch;

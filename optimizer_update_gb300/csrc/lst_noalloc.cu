@@ -16,7 +16,7 @@
 namespace lst {
 
 // Scratch of the sum-of-squares reduction: a reserved 256-byte header and
-// one fp64 partial per (CTA, block) of one launch (1024 CTAs x 128 blocks):
+// one 8-byte partial sum per (CTA, block) of one launch (1024 CTAs x 128 blocks):
 // 1 MiB + 256 bytes per device.
 static __device__ __align__(256) unsigned char g_noalloc_workspace[kWorkspaceBytes];
 

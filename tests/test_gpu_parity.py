@@ -276,3 +276,19 @@ def test_zeros_signed_zeros_and_tiny_values_bit_exact(fmt, eps):
             assert np.array_equal(np.isnan(gf), np.isnan(ef)), f
             ok = ~np.isnan(ef)
             assert np.array_equal(got[f][ok], exp[f][ok]), f
+
+
+# ---- large launches with ragged blocks: blocks of 1, 9, 4097 and 70,001
+# elements (segments that end inside a warp's 256-element task span, padded)
+# in one launch with full TinyLlama-1.1B layers, above the small-launch
+# threshold: every element against the oracle, bit for bit.
+@pytest.mark.parametrize("fmt", ["L12", "L16M", "L16F"])
+@pytest.mark.parametrize("sgd", [False, True])
+def test_large_launch_ragged_blocks_full(fmt, sgd):
+    specs = [(n, sh, 0) for (n, sh, l) in shapes.tinyllama_full() if l == 1]
+    specs += [("one", (1,), 1), ("nine", (9,), 2), ("odd", (4097,), 2), ("big_odd", (70001,), 3)]
+    specs += [(n, sh, 4) for (n, sh, l) in shapes.tinyllama_full() if l == 2]
+    specs += [("tail", (2048 * 3 + 256,), 5)]
+    L, stats = _run_full(specs, fmt, "tinyllama_full_l16m" if fmt == "L16M" else "ragged_large", 7, sgd=sgd)
+    assert L.n_params * (22 if fmt == "L12" else 28) > (256 << 20)  # one large launch
+    _assert_bit_exact(stats)
