@@ -706,6 +706,22 @@ def link_bandwidth(torch, host_ptr_arrs, dev_a, dev_b, nbytes: int, reps: int = 
             "d2h_concurrent_gbs": d2h_conc, "bytes": nbytes}
 
 
+def copy_choice_summary(L):
+    """What the streamed steps' default copy mode (LST_COPY_AUTO) has learned:
+    sub-chunks timed, how many of them later steps move with the copy kernel
+    each way, and the slowest copy-engine sub-chunk rates it timed."""
+    cs = [L.stream_copy_choice(i) for i in range(L.n_layers)]
+    m = [c for c in cs if c["measured"]]
+    out = {"blocks_measured": len(m), "chunks": sum(c["chunks"] for c in m),
+           "kernel_in_chunks": sum(c["kernel_in_chunks"] for c in m),
+           "kernel_out_chunks": sum(c["kernel_out_chunks"] for c in m)}
+    h = [c["engine_h2d_gbs_min"] for c in m if c["engine_h2d_gbs_min"] > 0]
+    d = [c["engine_d2h_gbs_min"] for c in m if c["engine_d2h_gbs_min"] > 0]
+    out["engine_h2d_gbs_min"] = min(h) if h else None
+    out["engine_d2h_gbs_min"] = min(d) if d else None
+    return out
+
+
 def timed_launches(torch, stream, launch, steps, flush, flush_rd):
     """Per-launch device times (s) of `steps` launches, CUDA events on the
     launching stream around each, the L2 flushed before each when a flush
@@ -927,6 +943,17 @@ def run_ours(args):
         stream_call(t)
         t += 1
         pre.append(time.perf_counter() - t0w)
+    choice_before = copy_choice_summary(L)
+    # the same three steps with every sub-chunk on the copy engines (the mode
+    # that learns nothing), on the same allocations, for comparison
+    L.set_stream_copy(lst.LST_COPY_ENGINE, lst.LST_COPY_ENGINE)
+    pre_engine = []
+    for k in range(3):
+        t0w = time.perf_counter()
+        stream_call(t)
+        t += 1
+        pre_engine.append(time.perf_counter() - t0w)
+    L.set_stream_copy(lst.LST_COPY_AUTO, lst.LST_COPY_AUTO)
     rates_before = block_link_rates(torch, arrs, buf0)
     roof_before = max(h2d_b / (link_before["h2d_concurrent_gbs"] * 1e9),
                       d2h_b / (link_before["d2h_concurrent_gbs"] * 1e9))
@@ -935,6 +962,10 @@ def run_ours(args):
                        "frac_of_link_roofline": roof_before / statistics.median(pre),
                        "note": "first three calls on the pinned blocks as allocated (lst_host_alloc), "
                                "before slow allocations are replaced",
+                       "copy_choice": choice_before,
+                       "copy_engines_only": {"step_ms": [1e3 * x for x in pre_engine],
+                                             "median_step_ms": 1e3 * statistics.median(pre_engine),
+                                             "frac_of_link_roofline": roof_before / statistics.median(pre_engine)},
                        "block_h2d_gbs_min": min(rates_before[0]), "block_d2h_gbs_min": min(rates_before[1]),
                        "slow_blocks": sum(slow_block_flags(rates_before))}
     slow_before_heal, healed, retired = heal_pinned_state(torch, L, ptrs, arrs, buf0)
@@ -996,6 +1027,7 @@ def run_ours(args):
                        block_d2h_gbs_min=min(block_rates[1]), block_d2h_gbs_median=statistics.median(block_rates[1]),
                        slow_blocks=sum(slow_block_flags(block_rates)),
                        slow_blocks_before_heal=slow_before_heal, healed_blocks=healed,
+                       copy_choice=copy_choice_summary(L),
                        slow_blocks_before_timed_steps=slow_late, healed_before_timed_steps=healed_late,
                        link_before_heal={k: link_before[k] for k in ("h2d_gbs", "d2h_gbs", "h2d_concurrent_gbs",
                                                                      "d2h_concurrent_gbs")})

@@ -169,16 +169,43 @@ LST_API lst_status lst_layout_set_stream_chunk(lst_layout* layout, int64_t elems
      LST_COPY_ENGINE  cudaMemcpyAsync / cudaMemcpy2DAsync on the copy engines;
      LST_COPY_SM      a copy kernel on the same stream that reads or writes the
                       host block through its device mapping (pinned memory
-                      registered as mapped, e.g. from lst_host_alloc).
-   A host block without a device mapping is moved by the copy engines. Both
-   give identical bytes. Default: LST_COPY_ENGINE both ways (on GB300 the
-   fastest pipeline on a host whose pinned memory copies at the link rate: the
-   copy kernels compete with the update kernel for the SMs). On a host where
-   the copy engines read some pinned allocations at a few GB/s, LST_COPY_SM
-   both ways was several times faster; lst_zero_copy_step faster still.
-   LST_ERR_INVALID_ARG for another value. */
-typedef enum { LST_COPY_ENGINE = 0, LST_COPY_SM = 1 } lst_copy_mode;
+                      registered as mapped, e.g. from lst_host_alloc);
+     LST_COPY_AUTO    the copy engines, except for the sub-chunks of a host
+                      block that they moved slowly in an earlier streamed step:
+                      each step times every sub-chunk copy the copy engines
+                      make (events on the copy streams), and a sub-chunk of 4 MB
+                      or more that took longer than 2.5x its bytes at the best
+                      sub-chunk rate seen in its direction is moved by the copy
+                      kernel in the later steps, for as long as the block's host pointer, size
+                      and sub-chunk boundaries stay the same (setting the mode
+                      again forgets this). No extra copies are made.
+   A host block without a device mapping is moved by the copy engines. Every
+   mode gives identical bytes. Default: LST_COPY_AUTO both ways. On GB300 the
+   copy engines give the fastest pipeline on pinned memory they move at the
+   link rate (the copy kernels compete with the update kernel for the SMs);
+   on the shared hosts measured here, the copy engines move parts of some
+   pinned allocations at a few GB/s for their whole lifetime, while the copy
+   kernel still moves them at the link rate. lst_stream_copy_choice reports
+   what AUTO decided. LST_ERR_INVALID_ARG for another value. */
+typedef enum { LST_COPY_ENGINE = 0, LST_COPY_SM = 1, LST_COPY_AUTO = 2 } lst_copy_mode;
 LST_API lst_status lst_layout_set_stream_copy(lst_layout* layout, int32_t h2d_mode, int32_t d2h_mode);
+
+/* What LST_COPY_AUTO has learned about block `block` of this layout:
+   measured = 1 once a streamed step under LST_COPY_AUTO has timed the
+   block's copy-engine copies (for its current host pointer); chunks = its
+   sub-chunks in that step; kernel_in_chunks / kernel_out_chunks = how many of
+   them later steps move with the copy kernel (0 under LST_COPY_ENGINE, all
+   under LST_COPY_SM); and the slowest and fastest copy-engine sub-chunk rates
+   timed each way (GB/s, 0 where none). Host only.
+   Errors: LST_ERR_INVALID_ARG (null layout or out, block out of range). */
+typedef struct lst_copy_choice {
+  int32_t measured;
+  int32_t chunks;
+  int32_t kernel_in_chunks, kernel_out_chunks;
+  double engine_h2d_gbs_min, engine_h2d_gbs_max;
+  double engine_d2h_gbs_min, engine_d2h_gbs_max;
+} lst_copy_choice;
+LST_API lst_status lst_stream_copy_choice(const lst_layout* layout, int64_t block, lst_copy_choice* out);
 
 /* ------------------------------------------------------------------------
  * Device-resident step.
@@ -470,7 +497,10 @@ LST_API const char* lst_last_error(void);
    which it still drains its own work before returning). kind 3: committing
    block k-1 of a store (lst_store_write, lst_store_step) fails after its
    shadow file is written and flushed, before the rename, as a crash there
-   would. */
+   would. kind 4: LST_COPY_AUTO sees the copy-engine sub-chunk copies of
+   every k-th block (blocks 0, k, 2k, ...; k >= 1) as 100x slower than they
+   were (nothing is slowed down), as on a host whose pinned memory the copy
+   engines move slowly in places. */
 LST_API lst_status lst_test_inject(int32_t kind, int64_t k);
 
 #ifdef __cplusplus

@@ -303,8 +303,9 @@ extern "C" const char* lst_last_error(void) { return g_err; }
 
 extern "C" lst_status lst_test_inject(int32_t kind, int64_t k) {
   clear_error();
-  if (kind < 0 || kind > 3) return fail(LST_ERR_INVALID_ARG, "lst_test_inject: unknown kind %d", kind);
-  if ((kind == 1 || kind == 3) && k < 1) return fail(LST_ERR_INVALID_ARG, "lst_test_inject: k must be >= 1");
+  if (kind < 0 || kind > 4) return fail(LST_ERR_INVALID_ARG, "lst_test_inject: unknown kind %d", kind);
+  if ((kind == 1 || kind == 3 || kind == 4) && k < 1)
+    return fail(LST_ERR_INVALID_ARG, "lst_test_inject: k must be >= 1");
   inject().k.store(k);
   inject().kind.store(kind);
   return LST_OK;

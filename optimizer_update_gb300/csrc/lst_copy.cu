@@ -15,8 +15,10 @@
 // mixed-layout parameters) the copy kernels compete with the update kernel
 // for the SMs: on a host whose pinned memory copies at the link rate, copy
 // engines both ways 92 ms, SM copies in 111 ms, both ways 117 ms; on a host
-// with slow allocations 1.8-1.9 s, 1.4-1.6 s and 0.27-0.32 s. So the copy
-// engines are the default and this path an option (lst_layout_set_stream_copy).
+// with slow allocations 1.8-1.9 s, 1.4-1.6 s and 0.27-0.32 s. So the default
+// mode (LST_COPY_AUTO, lst_layout_set_stream_copy) keeps the copy engines and
+// takes this kernel only for a host block, and a direction, that the copy
+// engines move at under half this kernel's rate (measured per block).
 #include <mutex>
 
 #include "lst_internal.h"

@@ -48,6 +48,20 @@ struct Tensor {
 
 struct Engine;  // streamed-step resources (streams, events), per device
 
+// What LST_COPY_AUTO learned about one block's host memory: the sub-chunk
+// boundaries of the step that timed it, which sub-chunks the copy engines
+// moved at under 0.4 of the best sub-chunk rate seen (those go through the
+// copy kernel from then on), and the range of copy-engine rates timed. Valid
+// while the block's host pointer, size and sub-chunk boundaries stay the same.
+struct LinkChoice {
+  const void* host = nullptr;
+  int64_t bytes = 0;
+  std::vector<int64_t> cuts;
+  std::vector<uint8_t> slow_in, slow_out;
+  bool measured = false;
+  double engine_h2d_min = 0, engine_h2d_max = 0, engine_d2h_min = 0, engine_d2h_max = 0;  // GB/s
+};
+
 }  // namespace lst
 
 struct lst_layout {
@@ -55,8 +69,9 @@ struct lst_layout {
   int64_t n_params = 0;
   int64_t max_block_bytes = 0;
   int64_t stream_chunk = lst::kDefaultStreamChunk;
-  int stream_copy_h2d = LST_COPY_ENGINE;  // how the streamed steps move sub-chunks in
-  int stream_copy_d2h = LST_COPY_ENGINE;  // ... and out (lst_layout_set_stream_copy)
+  int stream_copy_h2d = LST_COPY_AUTO;  // how the streamed steps move sub-chunks in
+  int stream_copy_d2h = LST_COPY_AUTO;  // ... and out (lst_layout_set_stream_copy)
+  std::vector<lst::LinkChoice> link;    // per block, for LST_COPY_AUTO
   std::vector<lst::Block> blocks;
   std::vector<lst::Tensor> tensors;
   std::mutex stream_mu;           // serialises lst_stream_step on this layout

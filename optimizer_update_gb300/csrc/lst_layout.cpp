@@ -227,12 +227,41 @@ extern "C" lst_status lst_layout_transfer(const lst_layout* L, int64_t layer, in
 extern "C" lst_status lst_layout_set_stream_copy(lst_layout* L, int32_t h2d_mode, int32_t d2h_mode) {
   clear_error();
   if (!L) return fail(LST_ERR_INVALID_ARG, "lst_layout_set_stream_copy: null layout");
-  auto ok = [](int32_t m) { return m == LST_COPY_ENGINE || m == LST_COPY_SM; };
+  auto ok = [](int32_t m) { return m == LST_COPY_ENGINE || m == LST_COPY_SM || m == LST_COPY_AUTO; };
   if (!ok(h2d_mode) || !ok(d2h_mode))
-    return fail(LST_ERR_INVALID_ARG, "lst_layout_set_stream_copy: mode must be LST_COPY_ENGINE or LST_COPY_SM");
+    return fail(LST_ERR_INVALID_ARG,
+                "lst_layout_set_stream_copy: mode must be LST_COPY_ENGINE, LST_COPY_SM or LST_COPY_AUTO");
   std::lock_guard<std::mutex> g(L->stream_mu);
   L->stream_copy_h2d = h2d_mode;
   L->stream_copy_d2h = d2h_mode;
+  L->link.clear();  // LST_COPY_AUTO measures again
+  return LST_OK;
+}
+
+extern "C" lst_status lst_stream_copy_choice(const lst_layout* Lc, int64_t block, lst_copy_choice* out) {
+  clear_error();
+  if (!Lc || !out) return fail(LST_ERR_INVALID_ARG, "lst_stream_copy_choice: null argument");
+  if (block < 0 || block >= (int64_t)Lc->blocks.size())
+    return fail(LST_ERR_INVALID_ARG, "lst_stream_copy_choice: block %lld out of range", (long long)block);
+  lst_layout* L = const_cast<lst_layout*>(Lc);  // the lock only
+  std::lock_guard<std::mutex> g(L->stream_mu);
+  lst_copy_choice c{};
+  if ((size_t)block < L->link.size() && L->link[(size_t)block].measured) {
+    const LinkChoice& k = L->link[(size_t)block];
+    c.measured = 1;
+    c.chunks = (int32_t)k.slow_in.size();
+    for (size_t j = 0; j < k.slow_in.size(); ++j) {
+      c.kernel_in_chunks += k.slow_in[j] ? 1 : 0;
+      c.kernel_out_chunks += k.slow_out[j] ? 1 : 0;
+    }
+    c.engine_h2d_gbs_min = k.engine_h2d_min;
+    c.engine_h2d_gbs_max = k.engine_h2d_max;
+    c.engine_d2h_gbs_min = k.engine_d2h_min;
+    c.engine_d2h_gbs_max = k.engine_d2h_max;
+  }
+  if (L->stream_copy_h2d != LST_COPY_AUTO) c.kernel_in_chunks = L->stream_copy_h2d == LST_COPY_SM ? c.chunks : 0;
+  if (L->stream_copy_d2h != LST_COPY_AUTO) c.kernel_out_chunks = L->stream_copy_d2h == LST_COPY_SM ? c.chunks : 0;
+  *out = c;
   return LST_OK;
 }
 

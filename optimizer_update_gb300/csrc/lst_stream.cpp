@@ -40,6 +40,11 @@ struct Engine {
   cudaEvent_t buffer_free[2] = {nullptr, nullptr};
   cudaEvent_t done = nullptr;
   size_t max_pitch = 0;  // the device's largest pitch for 2D copies
+  // LST_COPY_AUTO: timing events around the copy-engine sub-chunk copies
+  // (grown as needed, reused by every step), and the best sub-chunk rate
+  // seen each way (GB/s: 0 inbound, 1 outbound)
+  std::vector<cudaEvent_t> timers;
+  double best_gbs[2] = {0.0, 0.0};
 };
 
 static void release(Engine* e) {
@@ -49,6 +54,8 @@ static void release(Engine* e) {
     if (e->buffer_free[b]) cudaEventDestroy(e->buffer_free[b]);
   }
   if (e->done) cudaEventDestroy(e->done);
+  for (cudaEvent_t t : e->timers) cudaEventDestroy(t);
+  e->timers.clear();
   if (e->h2d) cudaStreamDestroy(e->h2d);
   if (e->compute) cudaStreamDestroy(e->compute);
   if (e->d2h) cudaStreamDestroy(e->d2h);
@@ -242,6 +249,65 @@ static cudaError_t enqueue_range(Enqueuer& enq, const Engine* E, const FormatInf
   return cudaSuccess;
 }
 
+// LST_COPY_AUTO: one timed copy-engine sub-chunk copy of a step.
+struct ChunkTiming {
+  int64_t block;
+  int chunk;
+  int dir;  // 0 inbound, 1 outbound
+  size_t ev;  // timers[ev] before the copies, timers[ev + 1] after
+  int64_t bytes;
+};
+
+static cudaError_t timer_pair(Engine* E, size_t* at, size_t* next) {
+  while (E->timers.size() < *next + 2) {
+    cudaEvent_t t = nullptr;
+    const cudaError_t err = cudaEventCreateWithFlags(&t, cudaEventDefault);
+    if (err != cudaSuccess) return err;
+    E->timers.push_back(t);
+  }
+  *at = *next;
+  *next += 2;
+  return cudaSuccess;
+}
+
+// After a completed step: the rate of every timed sub-chunk copy; a
+// sub-chunk whose copy took longer than its bytes at 0.4 of the best rate
+// seen in its direction goes through the copy kernel from the next step on.
+// (A slow part of a pinned allocation moves at 3-56 GB/s where the rest moves
+// at 165-210; the threshold sits well between.) Copies under 4 MB are timed
+// but neither set the best rate nor count as slow: a copy's fixed cost of a
+// few microseconds dominates them.
+constexpr int64_t kMinJudgedCopy = int64_t(4) << 20;
+
+static void learn_from_timings(lst_layout* L, Engine* E, const std::vector<ChunkTiming>& timed) {
+  const int inject_every = inject().kind.load() == 4 ? (int)inject().k.load() : 0;
+  std::vector<double> gbs(timed.size(), -1.0);
+  for (size_t j = 0; j < timed.size(); ++j) {
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, E->timers[timed[j].ev], E->timers[timed[j].ev + 1]) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (ms <= 0.0f) continue;
+    double r = (double)timed[j].bytes / (ms * 1e-3) / 1e9;
+    if (inject_every > 0 && timed[j].block % inject_every == 0) r /= 100.0;  // test hook
+    gbs[j] = r;
+    if (timed[j].bytes >= kMinJudgedCopy && r > E->best_gbs[timed[j].dir]) E->best_gbs[timed[j].dir] = r;
+  }
+  for (size_t j = 0; j < timed.size(); ++j) {
+    if (gbs[j] < 0.0) continue;
+    const ChunkTiming& t = timed[j];
+    LinkChoice& c = L->link[(size_t)t.block];
+    c.measured = true;
+    double& lo = t.dir == 0 ? c.engine_h2d_min : c.engine_d2h_min;
+    double& hi = t.dir == 0 ? c.engine_h2d_max : c.engine_d2h_max;
+    if (lo == 0.0 || gbs[j] < lo) lo = gbs[j];
+    if (gbs[j] > hi) hi = gbs[j];
+    if (t.bytes >= kMinJudgedCopy && gbs[j] < 0.4 * E->best_gbs[t.dir])
+      (t.dir == 0 ? c.slow_in : c.slow_out)[(size_t)t.chunk] = 1;
+  }
+}
+
 static void drain(Engine* e) {
   cudaStreamSynchronize(e->h2d);
   cudaStreamSynchronize(e->compute);
@@ -354,8 +420,17 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
   Engine* E = L->engine;
 
   const FormatInfo& fi = format_info(L->fmt);
-  Enqueuer enq{inject().kind.load(), inject().k.load()};
   char* bufs[2] = {static_cast<char*>(dev_buf0), static_cast<char*>(dev_buf1)};
+
+  // LST_COPY_AUTO: per block, what earlier steps learned about its host
+  // memory (reset where the pointer or size changed); this step times its
+  // copy-engine sub-chunk copies.
+  const bool auto_in = L->stream_copy_h2d == LST_COPY_AUTO;
+  const bool auto_out = L->stream_copy_d2h == LST_COPY_AUTO;
+  if ((auto_in || auto_out) && L->link.size() != (size_t)n) L->link.assign((size_t)n, LinkChoice());
+  std::vector<ChunkTiming> timed;
+  size_t next_timer = 0;
+  Enqueuer enq{inject().kind.load(), inject().k.load()};
   bool used[2] = {false, false};
   const char* what = nullptr;
 
@@ -387,10 +462,7 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
     char* buf = bufs[bi];
     char* host = static_cast<char*>(host_blocks[i]);
     // the SMs reach the host block through its device mapping
-    const bool sm_in = L->stream_copy_h2d == LST_COPY_SM && mapped[(size_t)i];
-    const bool sm_out = L->stream_copy_d2h == LST_COPY_SM && mapped[(size_t)i];
-    char* host_in = sm_in ? mapped[(size_t)i] : host;
-    char* host_out = sm_out ? mapped[(size_t)i] : host;
+    const bool has_map = mapped[(size_t)i] != nullptr;
     if (used[bi]) {  // buffer-free: the last outbound copy from this buffer
       RecordOp w{E->buffer_free[bi], E->h2d};
       if ((err = enq(do_wait, &w)) != cudaSuccess) { what = "wait buffer-free"; break; }
@@ -403,8 +475,28 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
     const int64_t C = (L->stream_chunk > 0 && L->stream_chunk < b.padded) ? L->stream_chunk : b.padded;
     const bool whole = (C == b.padded);
     const std::vector<int64_t> cuts = chunk_cuts(b.padded, C, i == first_active, i == last_active);
+    LinkChoice* lc = (auto_in || auto_out) ? &L->link[(size_t)i] : nullptr;
+    if (lc && (lc->host != host_blocks[i] || lc->bytes != b.bytes || lc->cuts != cuts)) {
+      *lc = LinkChoice();  // new memory or new sub-chunks: nothing learned yet
+      lc->host = host_blocks[i];
+      lc->bytes = b.bytes;
+      lc->cuts = cuts;
+      lc->slow_in.assign(cuts.size() - 1, 0);
+      lc->slow_out.assign(cuts.size() - 1, 0);
+    }
     for (size_t ci = 0; ci + 1 < cuts.size(); ++ci) {
       const int64_t e0 = cuts[ci], e1 = cuts[ci + 1];
+      const bool sm_in = has_map && (L->stream_copy_h2d == LST_COPY_SM || (auto_in && lc->slow_in[ci]));
+      const bool sm_out = has_map && (L->stream_copy_d2h == LST_COPY_SM || (auto_out && lc->slow_out[ci]));
+      char* host_in = sm_in ? mapped[(size_t)i] : host;
+      char* host_out = sm_out ? mapped[(size_t)i] : host;
+      const bool time_in = auto_in && !sm_in, time_out = auto_out && !sm_out;
+      size_t ev_in = 0, ev_out = 0;
+      if (time_in) {
+        if ((err = timer_pair(E, &ev_in, &next_timer)) != cudaSuccess) { what = "timing event"; break; }
+        RecordOp r0{E->timers[ev_in], E->h2d};
+        if ((err = enq(do_record, &r0)) != cudaSuccess) { what = "record timing"; break; }
+      }
       // StreamIn: the fields the update reads (all but G when the gradient is
       // already on the device; G is the first segment, so the rest is one range).
       const int first_in = dev_grads ? 1 : 0;
@@ -424,6 +516,13 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
                             E->h2d, sm_in);
         if (err != cudaSuccess) { what = "copy in"; break; }
       }
+      if (time_in) {
+        RecordOp r0{E->timers[ev_in + 1], E->h2d};
+        if ((err = enq(do_record, &r0)) != cudaSuccess) { what = "record timing"; break; }
+        int64_t nb = 0;
+        for (int k = first_in; k < fi.n_inputs; ++k) nb += (e1 - e0) * fi.elem_bytes[k];
+        timed.push_back(ChunkTiming{i, (int)ci, 0, ev_in, nb});
+      }
       RecordOp r1{E->weights_ready[bi], E->h2d};
       if ((err = enq(do_record, &r1)) != cudaSuccess) { what = "record weights-ready"; break; }
       RecordOp w1{E->weights_ready[bi], E->compute};
@@ -442,6 +541,11 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
       if ((err = enq(do_record, &r2)) != cudaSuccess) { what = "record update-done"; break; }
       RecordOp w2{E->update_done[bi], E->d2h};
       if ((err = enq(do_wait, &w2)) != cudaSuccess) { what = "wait update-done"; break; }
+      if (time_out) {
+        if ((err = timer_pair(E, &ev_out, &next_timer)) != cudaSuccess) { what = "timing event"; break; }
+        RecordOp r0{E->timers[ev_out], E->d2h};
+        if ((err = enq(do_record, &r0)) != cudaSuccess) { what = "record timing"; break; }
+      }
       // StreamOut: the fields the update wrote.
       if (whole) {
         const size_t nb = (size_t)b.d2h_bytes;
@@ -457,6 +561,13 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
         err = enqueue_range(enq, E, fi, b, fi.first_output, fi.n_segments, e0, e1, host_out, buf,
                             cudaMemcpyDeviceToHost, E->d2h, sm_out);
         if (err != cudaSuccess) { what = "copy out"; break; }
+      }
+      if (time_out) {
+        RecordOp r0{E->timers[ev_out + 1], E->d2h};
+        if ((err = enq(do_record, &r0)) != cudaSuccess) { what = "record timing"; break; }
+        int64_t nb = 0;
+        for (int k = fi.first_output; k < fi.n_segments; ++k) nb += (e1 - e0) * fi.elem_bytes[k];
+        timed.push_back(ChunkTiming{i, (int)ci, 1, ev_out, nb});
       }
     }
     if (what) break;
@@ -480,7 +591,10 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
   const auto t0 = std::chrono::steady_clock::now();
   for (;;) {
     cudaError_t q = never_done ? cudaErrorNotReady : cudaEventQuery(E->done);
-    if (q == cudaSuccess) return LST_OK;
+    if (q == cudaSuccess) {
+      if (!timed.empty()) learn_from_timings(L, E, timed);
+      return LST_OK;
+    }
     if (q != cudaErrorNotReady) {
       drain(E);
       return cuda_fail(q, "lst_stream_step: waiting for completion");

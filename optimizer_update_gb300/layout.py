@@ -79,8 +79,13 @@ class Layout:
         lst.lst_layout_set_stream_chunk(self.handle, elems)
 
     def set_stream_copy(self, h2d_mode: int, d2h_mode: int) -> None:
-        """lst.LST_COPY_ENGINE or lst.LST_COPY_SM for each direction of the streamed steps."""
+        """lst.LST_COPY_ENGINE, lst.LST_COPY_SM or lst.LST_COPY_AUTO (the default)
+        for each direction of the streamed steps."""
         lst.lst_layout_set_stream_copy(self.handle, h2d_mode, d2h_mode)
+
+    def stream_copy_choice(self, layer: int) -> dict:
+        """What the streamed steps use for block `layer` (lst_stream_copy_choice)."""
+        return lst.lst_stream_copy_choice(self.handle, layer)
 
     # views ------------------------------------------------------------------
     def numpy_views(self, layer: int, buf):

@@ -44,6 +44,13 @@ class lst_adamw_hparams(ctypes.Structure):
                 ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64)]
 
 
+class lst_copy_choice(ctypes.Structure):
+    _fields_ = [("measured", ctypes.c_int32), ("chunks", ctypes.c_int32), ("kernel_in_chunks", ctypes.c_int32),
+                ("kernel_out_chunks", ctypes.c_int32), ("engine_h2d_gbs_min", ctypes.c_double),
+                ("engine_h2d_gbs_max", ctypes.c_double), ("engine_d2h_gbs_min", ctypes.c_double),
+                ("engine_d2h_gbs_max", ctypes.c_double)]
+
+
 class lst_step_options(ctypes.Structure):
     _fields_ = [("block_steps", ctypes.c_void_p), ("skip", ctypes.c_void_p), ("grad_sq", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p)]
@@ -101,6 +108,7 @@ def lib() -> ctypes.CDLL:
             "lst_layout_transfer": ([vp, i64, P(i64), P(i64), P(i64), P(i64)], ctypes.c_int),
             "lst_layout_set_stream_chunk": ([vp, i64], ctypes.c_int),
             "lst_layout_set_stream_copy": ([vp, i32, i32], ctypes.c_int),
+            "lst_stream_copy_choice": ([vp, i64, P(lst_copy_choice)], ctypes.c_int),
             "lst_adamw_step": ([vp, P(vp), P(lst_adamw_hparams), vp], ctypes.c_int),
             "lst_sgd_step": ([vp, P(vp), f32, vp], ctypes.c_int),
             "lst_stream_step": ([vp, P(vp), vp, vp, P(lst_adamw_hparams), i64], ctypes.c_int),
@@ -210,11 +218,20 @@ def lst_layout_set_stream_chunk(handle: int, elems: int) -> None:
     _check(lib().lst_layout_set_stream_chunk(handle, elems))
 
 
-LST_COPY_ENGINE, LST_COPY_SM = 0, 1
+LST_COPY_ENGINE, LST_COPY_SM, LST_COPY_AUTO = 0, 1, 2
 
 
 def lst_layout_set_stream_copy(handle: int, h2d_mode: int, d2h_mode: int) -> None:
     _check(lib().lst_layout_set_stream_copy(handle, h2d_mode, d2h_mode))
+
+
+def lst_stream_copy_choice(handle: int, block: int) -> dict:
+    """What LST_COPY_AUTO has learned about `block`: whether a streamed step
+    timed it, its sub-chunks, how many of them later steps move with the copy
+    kernel each way, and the copy-engine rates timed (GB/s, 0 where none)."""
+    c = lst_copy_choice()
+    _check(lib().lst_stream_copy_choice(handle, block, ctypes.byref(c)))
+    return {f: (bool(getattr(c, f)) if f == "measured" else getattr(c, f)) for f, _ in c._fields_}
 
 
 def lst_adamw_step(handle: int, dev_blocks: Sequence[int], hparams: lst_adamw_hparams, stream: int = 0) -> None:

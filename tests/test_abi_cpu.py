@@ -99,15 +99,20 @@ def test_geometry_queries_reject_out_of_range(L):
         for call in (lambda: L.lst_layout_block(h, 1), lambda: L.lst_layout_segment(h, 0, "MASTER"),
                      lambda: L.lst_layout_tensor(h, 1, "G"), lambda: L.lst_layout_transfer(h, -1),
                      lambda: L.lst_layout_set_stream_chunk(h, 1000),
-                     lambda: L.lst_layout_set_stream_copy(h, 2, 0), lambda: L.lst_layout_set_stream_copy(h, 0, -1)):
+                     lambda: L.lst_layout_set_stream_copy(h, 3, 0), lambda: L.lst_layout_set_stream_copy(h, 0, -1),
+                     lambda: L.lst_stream_copy_choice(h, 1), lambda: L.lst_stream_copy_choice(h, -1)):
             with pytest.raises(L.LstError) as e:
                 call()
             assert e.value.status == L.LST_ERR_INVALID_ARG
         L.lst_layout_set_stream_chunk(h, 4096)
         L.lst_layout_set_stream_chunk(h, 0)
-        for a in (L.LST_COPY_ENGINE, L.LST_COPY_SM):
-            for b in (L.LST_COPY_ENGINE, L.LST_COPY_SM):
+        # no streamed step has timed the block yet: nothing learned
+        c = L.lst_stream_copy_choice(h, 0)
+        assert not c["measured"] and c["chunks"] == 0 and c["kernel_in_chunks"] == 0
+        for a in (L.LST_COPY_ENGINE, L.LST_COPY_SM, L.LST_COPY_AUTO):
+            for b in (L.LST_COPY_ENGINE, L.LST_COPY_SM, L.LST_COPY_AUTO):
                 L.lst_layout_set_stream_copy(h, a, b)
+                assert not L.lst_stream_copy_choice(h, 0)["measured"]
     finally:
         L.lst_layout_destroy(h)
 

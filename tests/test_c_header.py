@@ -40,7 +40,11 @@ int main(void) {
   /* streamed-step settings: sub-chunk size and copy mode per direction */
   int ok = lst_layout_set_stream_chunk(L, 4096) == LST_OK &&
            lst_layout_set_stream_copy(L, LST_COPY_SM, LST_COPY_ENGINE) == LST_OK &&
-           lst_layout_set_stream_copy(L, 2, LST_COPY_ENGINE) == LST_ERR_INVALID_ARG;
+           lst_layout_set_stream_copy(L, LST_COPY_AUTO, LST_COPY_AUTO) == LST_OK &&
+           lst_layout_set_stream_copy(L, 3, LST_COPY_ENGINE) == LST_ERR_INVALID_ARG;
+  lst_copy_choice cc;
+  ok = ok && lst_stream_copy_choice(L, 0, &cc) == LST_OK && cc.measured == 0 && cc.kernel_in_chunks == 0 &&
+       lst_stream_copy_choice(L, 99, &cc) == LST_ERR_INVALID_ARG;
   printf("%d\n", ok);
   lst_layout_destroy(L);
   return 0;
