@@ -195,8 +195,9 @@ LST_API lst_status lst_layout_set_stream_copy(lst_layout* layout, int32_t h2d_mo
    block's copy-engine copies (for its current host pointer); chunks = its
    sub-chunks in that step; kernel_in_chunks / kernel_out_chunks = how many of
    them later steps move with the copy kernel (0 under LST_COPY_ENGINE, all
-   under LST_COPY_SM); and the slowest and fastest copy-engine sub-chunk rates
-   timed each way (GB/s, 0 where none). Host only.
+   under LST_COPY_SM); and the slowest and fastest rates of its copy-engine
+   sub-chunk copies of 4 MB or more timed each way (GB/s, 0 where none).
+   Host only.
    Errors: LST_ERR_INVALID_ARG (null layout or out, block out of range). */
 typedef struct lst_copy_choice {
   int32_t measured;

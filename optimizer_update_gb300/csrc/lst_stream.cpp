@@ -299,12 +299,12 @@ static void learn_from_timings(lst_layout* L, Engine* E, const std::vector<Chunk
     const ChunkTiming& t = timed[j];
     LinkChoice& c = L->link[(size_t)t.block];
     c.measured = true;
+    if (t.bytes < kMinJudgedCopy) continue;
     double& lo = t.dir == 0 ? c.engine_h2d_min : c.engine_d2h_min;
     double& hi = t.dir == 0 ? c.engine_h2d_max : c.engine_d2h_max;
     if (lo == 0.0 || gbs[j] < lo) lo = gbs[j];
     if (gbs[j] > hi) hi = gbs[j];
-    if (t.bytes >= kMinJudgedCopy && gbs[j] < 0.4 * E->best_gbs[t.dir])
-      (t.dir == 0 ? c.slow_in : c.slow_out)[(size_t)t.chunk] = 1;
+    if (gbs[j] < 0.4 * E->best_gbs[t.dir]) (t.dir == 0 ? c.slow_in : c.slow_out)[(size_t)t.chunk] = 1;
   }
 }
 

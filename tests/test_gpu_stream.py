@@ -121,7 +121,8 @@ def _auto_state(L):
 @pytest.mark.parametrize("fmt,workload", FMTS)
 def test_stream_auto_copy_default_bit_identical(fmt, workload):
     """The default mode, two steps: the same bytes as the device-resident
-    step; every block timed, with positive rates each way."""
+    step; every block timed, with positive rates each way (its sub-chunks
+    are 12 MB or more)."""
     L = _stream_vs_device(_three_tinyllama_layers(), fmt, workload, 10, 1 << 20, steps=2)
     for i, c in enumerate(_auto_state(L)):
         assert c["measured"] and c["chunks"] >= 1, (i, c)
