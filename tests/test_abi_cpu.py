@@ -274,3 +274,35 @@ def test_bench_reference_arm_uses_only_the_oracle_and_the_generator():
     assert line["config"]["name"] == "llama70b_slice8_l12"
     assert "first" in line["cpu_baseline"]["sample"]
     assert lines[-1] == "LOADED False False"
+
+
+def test_bench_health_check_flags_either_direction():
+    """The bench's pinned-state health check: a block counts as slow when
+    either direction is under 0.85 of the best block's rate in that direction."""
+    import bench
+    h2d = [210.0, 200.0, 20.0, 209.0]
+    d2h = [193.0, 150.0, 193.0, 192.0]
+    assert bench.slow_block_flags((h2d, d2h)) == [False, True, True, False]
+    assert bench.slow_block_flags((h2d, d2h), frac=0.7) == [False, False, True, False]
+
+
+def test_bench_copy_choice_summary_adds_up_blocks():
+    """The bench's summary of what the default copy mode learned: sums over
+    the measured blocks, minima over the rates that were timed."""
+    import bench
+
+    class FakeLayout:
+        n_layers = 3
+        _c = [dict(measured=True, chunks=10, kernel_in_chunks=2, kernel_out_chunks=0, engine_h2d_gbs_min=4.5,
+                   engine_h2d_gbs_max=200.0, engine_d2h_gbs_min=150.0, engine_d2h_gbs_max=190.0),
+              dict(measured=False, chunks=0, kernel_in_chunks=0, kernel_out_chunks=0, engine_h2d_gbs_min=0.0,
+                   engine_h2d_gbs_max=0.0, engine_d2h_gbs_min=0.0, engine_d2h_gbs_max=0.0),
+              dict(measured=True, chunks=4, kernel_in_chunks=4, kernel_out_chunks=1, engine_h2d_gbs_min=0.0,
+                   engine_h2d_gbs_max=0.0, engine_d2h_gbs_min=120.0, engine_d2h_gbs_max=180.0)]
+
+        def stream_copy_choice(self, i):
+            return self._c[i]
+
+    s = bench.copy_choice_summary(FakeLayout())
+    assert s == {"blocks_measured": 2, "chunks": 14, "kernel_in_chunks": 6, "kernel_out_chunks": 1,
+                 "engine_h2d_gbs_min": 4.5, "engine_d2h_gbs_min": 120.0}
