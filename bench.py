@@ -995,6 +995,11 @@ def run_ours(args):
     if healed_late:
         block_rates = block_link_rates(torch, arrs, buf0)
     step_times = []
+    # sub-chunks the timed steps move with the SM copy kernel (what the
+    # default copy mode learned so far): one copy-kernel launch per run of
+    # equal-width segments (two per direction, one for the fp32 layout)
+    cc_timed = copy_choice_summary(L)
+    sm_launches = (1 if L.fmt == "L16F" else 2) * (cc_timed["kernel_in_chunks"] + cc_timed["kernel_out_chunks"])
     for k in range(n_stream):
         tt = t_first + k
         if args.workload in FRESH_GRAD_STEPS and k > 0:
@@ -1104,7 +1109,7 @@ def run_ours(args):
                          "back_to_back_l2_warm": res["back_to_back_l2_warm"]},
             "e2e": {"value": e2e_value, "unit": "params/s", "h2d_bytes_per_step": h2d_b,
                     "d2h_bytes_per_step": d2h_b, "steps": n_stream, "call": "lst_stream_step",
-                    "gpu_launches": n_stream * chunks},
+                    "gpu_launches": n_stream * (chunks + sm_launches)},
             "e2e_before_heal": e2e_before_heal,
             "options": options,
             "sgd": sgd,
