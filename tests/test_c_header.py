@@ -81,3 +81,54 @@ def test_c99_program_uses_the_abi(libdir, tmp_path):
     assert nums[8:10] == [2 * 2048 + 32 * 4, 32]
     assert out[1].startswith("1 invalid argument")
     assert out[2] == "1"
+
+
+STRUCT_PROGRAM = r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "lst.h"
+#define F(T, f) printf(#T " " #f " %zu %zu\n", offsetof(T, f), sizeof(((T*)0)->f))
+int main(void) {
+  printf("lst_adamw_hparams - %zu 0\n", sizeof(lst_adamw_hparams));
+  F(lst_adamw_hparams, lr); F(lst_adamw_hparams, beta1); F(lst_adamw_hparams, beta2);
+  F(lst_adamw_hparams, eps); F(lst_adamw_hparams, weight_decay); F(lst_adamw_hparams, step);
+  printf("lst_step_options - %zu 0\n", sizeof(lst_step_options));
+  F(lst_step_options, block_steps); F(lst_step_options, skip); F(lst_step_options, grad_sq);
+  F(lst_step_options, workspace);
+  printf("lst_copy_choice - %zu 0\n", sizeof(lst_copy_choice));
+  F(lst_copy_choice, measured); F(lst_copy_choice, chunks); F(lst_copy_choice, kernel_in_chunks);
+  F(lst_copy_choice, kernel_out_chunks); F(lst_copy_choice, engine_h2d_gbs_min);
+  F(lst_copy_choice, engine_h2d_gbs_max); F(lst_copy_choice, engine_d2h_gbs_min);
+  F(lst_copy_choice, engine_d2h_gbs_max);
+  return 0;
+}
+"""
+
+
+def test_c_structs_match_the_binding(tmp_path):
+    """Every public struct of include/lst.h has the size, field offsets and
+    field sizes that the ctypes binding declares."""
+    import ctypes
+    from optimizer_update_gb300 import lst
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "structs.c"
+    src.write_text(STRUCT_PROGRAM)
+    exe = tmp_path / "structs"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                    str(exe)], check=True)
+    lines = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    seen = set()
+    for line in filter(None, lines):
+        name, field, off, size = line.split()
+        T = getattr(lst, name)
+        if field == "-":
+            assert ctypes.sizeof(T) == int(off), name
+            continue
+        d = getattr(T, field)
+        assert (d.offset, d.size) == (int(off), int(size)), (name, field)
+        seen.add((name, field))
+    for name in ("lst_adamw_hparams", "lst_step_options", "lst_copy_choice"):
+        fields = {f for f, _ in getattr(lst, name)._fields_ if not f.endswith("_")}
+        assert fields == {f for n, f in seen if n == name}, name
