@@ -171,22 +171,23 @@ LST_API lst_status lst_layout_set_stream_chunk(lst_layout* layout, int64_t elems
                       host block through its device mapping (pinned memory
                       registered as mapped, e.g. from lst_host_alloc);
      LST_COPY_AUTO    the copy engines, except for the sub-chunks of a host
-                      block that they moved slowly in an earlier streamed step:
-                      each step times every sub-chunk copy the copy engines
-                      make (events on the copy streams), and a sub-chunk of 4 MB
-                      or more that took longer than 2.5x its bytes at the best
-                      sub-chunk rate seen in its direction is moved by the copy
-                      kernel in the later steps, for as long as the block's host pointer, size
-                      and sub-chunk boundaries stay the same (setting the mode
-                      again forgets this). No extra copies are made.
+                      block that they moved slowly in an earlier streamed
+                      step. Each step times every sub-chunk copy the copy
+                      engines make (events on the copy streams); a sub-chunk
+                      of 4 MB or more that took longer than 2.5x its bytes at
+                      the best sub-chunk rate seen in its direction is moved
+                      by the copy kernel in the later steps, for as long as
+                      the block's host pointer, size and sub-chunk boundaries
+                      stay the same (setting the mode again forgets this). No
+                      extra copies are made.
    A host block without a device mapping is moved by the copy engines. Every
    mode gives identical bytes. Default: LST_COPY_AUTO both ways. On GB300 the
    copy engines give the fastest pipeline on pinned memory they move at the
    link rate (the copy kernels compete with the update kernel for the SMs);
    on the shared hosts measured here, the copy engines move parts of some
-   pinned allocations at a few GB/s for their whole lifetime, while the copy
-   kernel still moves them at the link rate. lst_stream_copy_choice reports
-   what AUTO decided. LST_ERR_INVALID_ARG for another value. */
+   pinned allocations at a few GB/s for their whole lifetime, and the copy
+   kernel moved such parts faster. lst_stream_copy_choice reports what AUTO
+   decided. LST_ERR_INVALID_ARG for another value. */
 typedef enum { LST_COPY_ENGINE = 0, LST_COPY_SM = 1, LST_COPY_AUTO = 2 } lst_copy_mode;
 LST_API lst_status lst_layout_set_stream_copy(lst_layout* layout, int32_t h2d_mode, int32_t d2h_mode);
 
