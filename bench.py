@@ -294,6 +294,28 @@ def build_layout(workload: str, max_blocks: int = 0):
     return Layout(workload_specs(workload, max_blocks), WORKLOADS[workload][1])
 
 
+def host_mem_available() -> int:
+    """MemAvailable of /proc/meminfo in bytes (0 if it cannot be read)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def replicas_fit(state_bytes: int, local_ranks: int, available: int, heal_extra: int = 40 << 30) -> bool:
+    """Whether one pinned copy of the state per rank on this host, plus the
+    health check's allowance for replacing slow allocations, fits in 3/4 of
+    the host's available memory (unknown availability: assume it does)."""
+    if available <= 0:
+        return True
+    per_rank = state_bytes + min(heal_extra, state_bytes // 2)
+    return local_ranks * per_rank <= 0.75 * available
+
+
 def rank_layout(workload: str, max_blocks: int, shard: bool, rank: int, world: int):
     """The layout this rank updates and the model index of its first block:
     the whole model (a replica), or with `shard` its contiguous range of the
@@ -877,6 +899,18 @@ def run_ours(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     dist_init("nccl")
+    # Replicas pin one copy of the state per rank; where the ranks on this
+    # host could not all hold one (82 GB each for the Llama-70B slice), they
+    # split the model's blocks instead (strong scaling). Decided together:
+    # any rank short of memory makes every rank shard.
+    auto_shard = False
+    if world > 1 and not args.shard:
+        full = build_layout(args.workload, args.max_blocks)
+        state = sum(full.block_bytes(i) for i in range(full.n_layers))
+        local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", world))
+        short = 0 if replicas_fit(state, local_ranks, host_mem_available()) else 1
+        if sum_over_ranks(short, device) > 0:
+            args.shard = auto_shard = True
     # replicas draw their own state; shards are parts of one model (one seed)
     seed = args.seed if args.shard else replica_seed(args.seed, rank)
 
@@ -968,7 +1002,8 @@ def run_ours(args):
                                              "frac_of_link_roofline": roof_before / statistics.median(pre_engine)},
                        "block_h2d_gbs_min": min(rates_before[0]), "block_d2h_gbs_min": min(rates_before[1]),
                        "slow_blocks": sum(slow_block_flags(rates_before))}
-    slow_before_heal, healed, retired = heal_pinned_state(torch, L, ptrs, arrs, buf0)
+    heal_budget = min(40 << 30, state_bytes // 2)  # as replicas_fit allows for
+    slow_before_heal, healed, retired = heal_pinned_state(torch, L, ptrs, arrs, buf0, max_extra_bytes=heal_budget)
     a0, a1 = probe_pair()
     link = link_bandwidth(torch, [a0, a1], buf0, buf1, nb)
 
@@ -990,7 +1025,8 @@ def run_ours(args):
     # slow pinned allocation holds up the pipeline): a block that has become
     # slow since the health check is replaced as well
     block_rates = block_link_rates(torch, arrs, buf0)
-    slow_late, healed_late, retired_late = heal_pinned_state(torch, L, ptrs, arrs, buf0, rates=block_rates)
+    slow_late, healed_late, retired_late = heal_pinned_state(torch, L, ptrs, arrs, buf0, rates=block_rates,
+                                                             max_extra_bytes=heal_budget)
     retired += retired_late
     if healed_late:
         block_rates = block_link_rates(torch, arrs, buf0)
@@ -1100,7 +1136,9 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": 1e3 * t_dev_max / args.steps, "higher_is_better": True,
             "scaling": "strong" if (args.shard and world > 1) else "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": layout_config(L, args.workload, world, args.max_blocks, args.shard, P_job),
+            "config": dict(layout_config(L, args.workload, world, args.max_blocks, args.shard, P_job),
+                           **({"sharded_because": "a pinned replica per rank would not fit in host memory"}
+                              if auto_shard else {})),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": f"{kname}<{L.fmt}>", "alg_bytes_per_launch": alg_bytes,

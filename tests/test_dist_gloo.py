@@ -121,3 +121,20 @@ def test_single_process_defaults():
         os.environ.pop(k, None)
     assert bench.dist_env() == (0, 0, 1)
     assert bench.max_over_ranks(3.25) == 3.25
+
+
+def test_replicas_fit_host_memory():
+    """The bench's guard for one pinned replica of the state per rank: the
+    state plus the health check's allowance, times the ranks on the host,
+    within 3/4 of the available memory; an unknown availability does not
+    block."""
+    import bench
+    GB = 1 << 30
+    state = 82 * GB   # the Llama-70B slice
+    assert bench.replicas_fit(state, 1, 200 * GB)          # one GPU on a ~200 GB host
+    assert not bench.replicas_fit(state, 2, 200 * GB)
+    assert bench.replicas_fit(state, 8, 1600 * GB)         # 8 x (82 + 40) = 976 GB
+    assert not bench.replicas_fit(state, 8, 1000 * GB)
+    assert bench.replicas_fit(state, 8, 0)
+    assert bench.replicas_fit(GB, 8, 64 * GB)              # small states: half the state as allowance
+    assert bench.host_mem_available() >= 0
