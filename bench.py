@@ -1069,6 +1069,7 @@ def run_ours(args):
                        slow_blocks=sum(slow_block_flags(block_rates)),
                        slow_blocks_before_heal=slow_before_heal, healed_blocks=healed,
                        copy_choice=copy_choice_summary(L),
+                       last_step=L.stream_last_stats(),
                        slow_blocks_before_timed_steps=slow_late, healed_before_timed_steps=healed_late,
                        link_before_heal={k: link_before[k] for k in ("h2d_gbs", "d2h_gbs", "h2d_concurrent_gbs",
                                                                      "d2h_concurrent_gbs")})

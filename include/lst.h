@@ -209,6 +209,24 @@ typedef struct lst_copy_choice {
 } lst_copy_choice;
 LST_API lst_status lst_stream_copy_choice(const lst_layout* layout, int64_t block, lst_copy_choice* out);
 
+/* The last streamed step on this layout that completed (lst_stream_step and
+   its variants, including those lst_store_step runs): steps_completed counts
+   them; h2d_bytes / d2h_bytes are the bytes it moved each way; chunks is its
+   sub-chunk count and kernel_in_chunks / kernel_out_chunks how many of them
+   the copy kernel moved; wall_ms is the host time from the call's first
+   enqueue to the completion it observed. Under LST_COPY_AUTO (timed = 1)
+   h2d_busy_ms / d2h_busy_ms are the summed durations of its copies each way
+   (events on the copy streams): with the link busy in both directions at
+   once, their sum exceeds wall_ms; 0 when not timed. All zero before the
+   first completed step. Host only. Errors: LST_ERR_INVALID_ARG (null). */
+typedef struct lst_stream_stats {
+  int64_t steps_completed;
+  int64_t h2d_bytes, d2h_bytes;
+  int32_t chunks, kernel_in_chunks, kernel_out_chunks, timed;
+  double wall_ms, h2d_busy_ms, d2h_busy_ms;
+} lst_stream_stats;
+LST_API lst_status lst_stream_last_stats(const lst_layout* layout, lst_stream_stats* out);
+
 /* ------------------------------------------------------------------------
  * Device-resident step.
  * ------------------------------------------------------------------------ */

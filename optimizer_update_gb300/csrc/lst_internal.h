@@ -72,6 +72,7 @@ struct lst_layout {
   int stream_copy_h2d = LST_COPY_AUTO;  // how the streamed steps move sub-chunks in
   int stream_copy_d2h = LST_COPY_AUTO;  // ... and out (lst_layout_set_stream_copy)
   std::vector<lst::LinkChoice> link;    // per block, for LST_COPY_AUTO
+  lst_stream_stats last_step{};         // the last streamed step that completed
   std::vector<lst::Block> blocks;
   std::vector<lst::Tensor> tensors;
   std::mutex stream_mu;           // serialises lst_stream_step on this layout

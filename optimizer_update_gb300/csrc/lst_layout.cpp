@@ -274,3 +274,12 @@ extern "C" lst_status lst_layout_set_stream_chunk(lst_layout* L, int64_t elems) 
   L->stream_chunk = elems;
   return LST_OK;
 }
+
+extern "C" lst_status lst_stream_last_stats(const lst_layout* Lc, lst_stream_stats* out) {
+  clear_error();
+  if (!Lc || !out) return fail(LST_ERR_INVALID_ARG, "lst_stream_last_stats: null argument");
+  lst_layout* L = const_cast<lst_layout*>(Lc);  // the lock only
+  std::lock_guard<std::mutex> g(L->stream_mu);
+  *out = L->last_step;
+  return LST_OK;
+}

@@ -256,6 +256,7 @@ struct ChunkTiming {
   int dir;  // 0 inbound, 1 outbound
   size_t ev;  // timers[ev] before the copies, timers[ev + 1] after
   int64_t bytes;
+  bool engine;  // moved by the copy engines (judged), else by the copy kernel
 };
 
 static cudaError_t timer_pair(Engine* E, size_t* at, size_t* next) {
@@ -282,13 +283,15 @@ constexpr int64_t kMinJudgedCopy = int64_t(4) << 20;
 static void learn_from_timings(lst_layout* L, Engine* E, const std::vector<ChunkTiming>& timed) {
   const int inject_every = inject().kind.load() == 4 ? (int)inject().k.load() : 0;
   std::vector<double> gbs(timed.size(), -1.0);
+  double busy_ms[2] = {0.0, 0.0};
   for (size_t j = 0; j < timed.size(); ++j) {
     float ms = 0.0f;
     if (cudaEventElapsedTime(&ms, E->timers[timed[j].ev], E->timers[timed[j].ev + 1]) != cudaSuccess) {
       cudaGetLastError();
       continue;
     }
-    if (ms <= 0.0f) continue;
+    busy_ms[timed[j].dir] += ms;
+    if (ms <= 0.0f || !timed[j].engine) continue;
     double r = (double)timed[j].bytes / (ms * 1e-3) / 1e9;
     if (inject_every > 0 && timed[j].block % inject_every == 0) r /= 100.0;  // test hook
     gbs[j] = r;
@@ -306,6 +309,8 @@ static void learn_from_timings(lst_layout* L, Engine* E, const std::vector<Chunk
     if (gbs[j] > hi) hi = gbs[j];
     if (gbs[j] < 0.4 * E->best_gbs[t.dir]) (t.dir == 0 ? c.slow_in : c.slow_out)[(size_t)t.chunk] = 1;
   }
+  L->last_step.h2d_busy_ms = busy_ms[0];
+  L->last_step.d2h_busy_ms = busy_ms[1];
 }
 
 static void drain(Engine* e) {
@@ -430,6 +435,8 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
   if ((auto_in || auto_out) && L->link.size() != (size_t)n) L->link.assign((size_t)n, LinkChoice());
   std::vector<ChunkTiming> timed;
   size_t next_timer = 0;
+  lst_stream_stats step{};
+  const auto t_start = std::chrono::steady_clock::now();
   Enqueuer enq{inject().kind.load(), inject().k.load()};
   bool used[2] = {false, false};
   const char* what = nullptr;
@@ -490,7 +497,15 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
       const bool sm_out = has_map && (L->stream_copy_d2h == LST_COPY_SM || (auto_out && lc->slow_out[ci]));
       char* host_in = sm_in ? mapped[(size_t)i] : host;
       char* host_out = sm_out ? mapped[(size_t)i] : host;
-      const bool time_in = auto_in && !sm_in, time_out = auto_out && !sm_out;
+      int64_t in_bytes = 0, out_bytes = 0;
+      for (int k = dev_grads ? 1 : 0; k < fi.n_inputs; ++k) in_bytes += (e1 - e0) * fi.elem_bytes[k];
+      for (int k = fi.first_output; k < fi.n_segments; ++k) out_bytes += (e1 - e0) * fi.elem_bytes[k];
+      step.h2d_bytes += in_bytes;
+      step.d2h_bytes += out_bytes;
+      step.chunks += 1;
+      step.kernel_in_chunks += sm_in ? 1 : 0;
+      step.kernel_out_chunks += sm_out ? 1 : 0;
+      const bool time_in = auto_in, time_out = auto_out;
       size_t ev_in = 0, ev_out = 0;
       if (time_in) {
         if ((err = timer_pair(E, &ev_in, &next_timer)) != cudaSuccess) { what = "timing event"; break; }
@@ -519,9 +534,7 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
       if (time_in) {
         RecordOp r0{E->timers[ev_in + 1], E->h2d};
         if ((err = enq(do_record, &r0)) != cudaSuccess) { what = "record timing"; break; }
-        int64_t nb = 0;
-        for (int k = first_in; k < fi.n_inputs; ++k) nb += (e1 - e0) * fi.elem_bytes[k];
-        timed.push_back(ChunkTiming{i, (int)ci, 0, ev_in, nb});
+        timed.push_back(ChunkTiming{i, (int)ci, 0, ev_in, in_bytes, !sm_in});
       }
       RecordOp r1{E->weights_ready[bi], E->h2d};
       if ((err = enq(do_record, &r1)) != cudaSuccess) { what = "record weights-ready"; break; }
@@ -565,9 +578,7 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
       if (time_out) {
         RecordOp r0{E->timers[ev_out + 1], E->d2h};
         if ((err = enq(do_record, &r0)) != cudaSuccess) { what = "record timing"; break; }
-        int64_t nb = 0;
-        for (int k = fi.first_output; k < fi.n_segments; ++k) nb += (e1 - e0) * fi.elem_bytes[k];
-        timed.push_back(ChunkTiming{i, (int)ci, 1, ev_out, nb});
+        timed.push_back(ChunkTiming{i, (int)ci, 1, ev_out, out_bytes, !sm_out});
       }
     }
     if (what) break;
@@ -592,6 +603,10 @@ static lst_status stream_impl(const lst_layout* Lc, void* const* host_blocks, vo
   for (;;) {
     cudaError_t q = never_done ? cudaErrorNotReady : cudaEventQuery(E->done);
     if (q == cudaSuccess) {
+      step.steps_completed = L->last_step.steps_completed + 1;
+      step.wall_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_start).count();
+      step.timed = timed.empty() ? 0 : 1;
+      L->last_step = step;
       if (!timed.empty()) learn_from_timings(L, E, timed);
       return LST_OK;
     }

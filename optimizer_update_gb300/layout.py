@@ -87,6 +87,10 @@ class Layout:
         """What the streamed steps use for block `layer` (lst_stream_copy_choice)."""
         return lst.lst_stream_copy_choice(self.handle, layer)
 
+    def stream_last_stats(self) -> dict:
+        """The last completed streamed step on this layout (lst_stream_last_stats)."""
+        return lst.lst_stream_last_stats(self.handle)
+
     # views ------------------------------------------------------------------
     def numpy_views(self, layer: int, buf):
         """Field -> numpy view over a host block (a uint8 numpy array of the block's size)."""

@@ -51,6 +51,13 @@ class lst_copy_choice(ctypes.Structure):
                 ("engine_d2h_gbs_max", ctypes.c_double)]
 
 
+class lst_stream_stats(ctypes.Structure):
+    _fields_ = [("steps_completed", ctypes.c_int64), ("h2d_bytes", ctypes.c_int64), ("d2h_bytes", ctypes.c_int64),
+                ("chunks", ctypes.c_int32), ("kernel_in_chunks", ctypes.c_int32), ("kernel_out_chunks", ctypes.c_int32),
+                ("timed", ctypes.c_int32), ("wall_ms", ctypes.c_double), ("h2d_busy_ms", ctypes.c_double),
+                ("d2h_busy_ms", ctypes.c_double)]
+
+
 class lst_step_options(ctypes.Structure):
     _fields_ = [("block_steps", ctypes.c_void_p), ("skip", ctypes.c_void_p), ("grad_sq", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p)]
@@ -109,6 +116,7 @@ def lib() -> ctypes.CDLL:
             "lst_layout_set_stream_chunk": ([vp, i64], ctypes.c_int),
             "lst_layout_set_stream_copy": ([vp, i32, i32], ctypes.c_int),
             "lst_stream_copy_choice": ([vp, i64, P(lst_copy_choice)], ctypes.c_int),
+            "lst_stream_last_stats": ([vp, P(lst_stream_stats)], ctypes.c_int),
             "lst_adamw_step": ([vp, P(vp), P(lst_adamw_hparams), vp], ctypes.c_int),
             "lst_sgd_step": ([vp, P(vp), f32, vp], ctypes.c_int),
             "lst_stream_step": ([vp, P(vp), vp, vp, P(lst_adamw_hparams), i64], ctypes.c_int),
@@ -232,6 +240,15 @@ def lst_stream_copy_choice(handle: int, block: int) -> dict:
     c = lst_copy_choice()
     _check(lib().lst_stream_copy_choice(handle, block, ctypes.byref(c)))
     return {f: (bool(getattr(c, f)) if f == "measured" else getattr(c, f)) for f, _ in c._fields_}
+
+
+def lst_stream_last_stats(handle: int) -> dict:
+    """The last completed streamed step on this layout: bytes moved each way,
+    sub-chunks (and how many the copy kernel moved), host wall time and, when
+    timed, the summed copy durations each way (ms)."""
+    st = lst_stream_stats()
+    _check(lib().lst_stream_last_stats(handle, ctypes.byref(st)))
+    return {f: getattr(st, f) for f, _ in st._fields_}
 
 
 def lst_adamw_step(handle: int, dev_blocks: Sequence[int], hparams: lst_adamw_hparams, stream: int = 0) -> None:

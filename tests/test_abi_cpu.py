@@ -106,6 +106,8 @@ def test_geometry_queries_reject_out_of_range(L):
             assert e.value.status == L.LST_ERR_INVALID_ARG
         L.lst_layout_set_stream_chunk(h, 4096)
         L.lst_layout_set_stream_chunk(h, 0)
+        # no streamed step has run: no statistics yet
+        assert L.lst_stream_last_stats(h) == {f: 0 for f, _ in L.lst_stream_stats._fields_}
         # no streamed step has timed the block yet: nothing learned
         c = L.lst_stream_copy_choice(h, 0)
         assert not c["measured"] and c["chunks"] == 0 and c["kernel_in_chunks"] == 0

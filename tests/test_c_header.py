@@ -100,6 +100,11 @@ int main(void) {
   F(lst_copy_choice, kernel_out_chunks); F(lst_copy_choice, engine_h2d_gbs_min);
   F(lst_copy_choice, engine_h2d_gbs_max); F(lst_copy_choice, engine_d2h_gbs_min);
   F(lst_copy_choice, engine_d2h_gbs_max);
+  printf("lst_stream_stats - %zu 0\n", sizeof(lst_stream_stats));
+  F(lst_stream_stats, steps_completed); F(lst_stream_stats, h2d_bytes); F(lst_stream_stats, d2h_bytes);
+  F(lst_stream_stats, chunks); F(lst_stream_stats, kernel_in_chunks); F(lst_stream_stats, kernel_out_chunks);
+  F(lst_stream_stats, timed); F(lst_stream_stats, wall_ms); F(lst_stream_stats, h2d_busy_ms);
+  F(lst_stream_stats, d2h_busy_ms);
   return 0;
 }
 """
@@ -129,6 +134,6 @@ def test_c_structs_match_the_binding(tmp_path):
         d = getattr(T, field)
         assert (d.offset, d.size) == (int(off), int(size)), (name, field)
         seen.add((name, field))
-    for name in ("lst_adamw_hparams", "lst_step_options", "lst_copy_choice"):
+    for name in ("lst_adamw_hparams", "lst_step_options", "lst_copy_choice", "lst_stream_stats"):
         fields = {f for f, _ in getattr(lst, name)._fields_ if not f.endswith("_")}
         assert fields == {f for n, f in seen if n == name}, name

@@ -124,6 +124,14 @@ def test_stream_auto_copy_default_bit_identical(fmt, workload):
     step; every block timed, with positive rates each way (its sub-chunks
     are 12 MB or more)."""
     L = _stream_vs_device(_three_tinyllama_layers(), fmt, workload, 10, 1 << 20, steps=2)
+    st = L.stream_last_stats()
+    assert st["steps_completed"] == 2 and st["timed"] == 1, st
+    assert st["h2d_bytes"] == sum(L.transfer(i)[1] for i in range(L.n_layers)), st
+    assert st["d2h_bytes"] == sum(L.transfer(i)[3] for i in range(L.n_layers)), st
+    assert st["chunks"] == sum(c["chunks"] for c in _auto_state(L)), st
+    # each direction's copies run one after another on their stream
+    for d in ("h2d", "d2h"):
+        assert 0 < st[f"{d}_busy_ms"] <= 1.05 * st["wall_ms"] + 0.5, st
     for i, c in enumerate(_auto_state(L)):
         assert c["measured"] and c["chunks"] >= 1, (i, c)
         assert c["kernel_in_chunks"] <= c["chunks"] and c["kernel_out_chunks"] <= c["chunks"]
