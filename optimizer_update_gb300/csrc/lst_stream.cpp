@@ -249,7 +249,9 @@ static cudaError_t enqueue_range(Enqueuer& enq, const Engine* E, const FormatInf
   return cudaSuccess;
 }
 
-// LST_COPY_AUTO: one timed copy-engine sub-chunk copy of a step.
+// LST_COPY_AUTO: one timed sub-chunk copy of a step (each direction of each
+// sub-chunk, by the copy engines or the copy kernel; only the copy engines'
+// copies are judged).
 struct ChunkTiming {
   int64_t block;
   int chunk;
@@ -271,7 +273,8 @@ static cudaError_t timer_pair(Engine* E, size_t* at, size_t* next) {
   return cudaSuccess;
 }
 
-// After a completed step: the rate of every timed sub-chunk copy; a
+// After a completed step: the summed copy time each way (the step's
+// statistics) and the rate of every timed copy-engine sub-chunk copy; a
 // sub-chunk whose copy took longer than its bytes at 0.4 of the best rate
 // seen in its direction goes through the copy kernel from the next step on.
 // (A slow part of a pinned allocation moves at 3-56 GB/s where the rest moves
